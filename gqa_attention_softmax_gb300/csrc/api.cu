@@ -1,0 +1,304 @@
+// C ABI of libsinkattn: argument validation, tensor-map encoding, launch
+// selection. Every entry point checks its arguments on the host before any
+// CUDA call and returns a status; nothing here allocates, frees or
+// synchronises (except the diagnostic sinkattn_debug_status).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+#include "sinkattn.h"
+
+namespace sinkattn {
+
+static thread_local char g_last_error[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
+                   int swizzle_bytes) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return SINKATTN_CUDA_ERROR;
+  }
+  if (rows == 0) rows = 1;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUtensorMapSwizzle sw =
+      swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return SINKATTN_CUDA_ERROR;
+  }
+  return SINKATTN_OK;
+}
+
+}  // namespace sinkattn
+
+using namespace sinkattn;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  set_error("%s", buf);
+  return status;
+}
+
+// Checks shared by every attention entry point.
+int check_common(const void* q, const void* k, const void* v, int32_t Hq, int32_t Hkv,
+                 int32_t d, float sm_scale, int32_t causal, int32_t window) {
+  if (!q || !k || !v) return fail(SINKATTN_INVALID_ARG, "q, k and v must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(SINKATTN_INVALID_ARG, "q, k and v must be 16-byte aligned");
+  if (Hq <= 0 || Hkv <= 0) return fail(SINKATTN_INVALID_ARG, "head counts must be positive");
+  if (Hq % Hkv != 0)
+    return fail(SINKATTN_UNSUPPORTED, "num_qo_heads (%d) is not a multiple of num_kv_heads (%d)",
+                Hq, Hkv);
+  if (d != 64 && d != 128) return fail(SINKATTN_UNSUPPORTED, "head_dim %d is not 64 or 128", d);
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale))
+    return fail(SINKATTN_INVALID_ARG, "sm_scale must be positive and finite");
+  if (causal != 0 && causal != 1) return fail(SINKATTN_INVALID_ARG, "causal must be 0 or 1");
+  if (window > 0 && !causal)
+    return fail(SINKATTN_UNSUPPORTED, "a sliding window requires causal masking");
+  return SINKATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sinkattn_status_string(int status) {
+  switch (status) {
+    case SINKATTN_OK: return "SINKATTN_OK";
+    case SINKATTN_INVALID_ARG: return "SINKATTN_INVALID_ARG";
+    case SINKATTN_UNSUPPORTED: return "SINKATTN_UNSUPPORTED";
+    case SINKATTN_CUDA_ERROR: return "SINKATTN_CUDA_ERROR";
+    case SINKATTN_TIMEOUT: return "SINKATTN_TIMEOUT";
+    case SINKATTN_BAD_LENGTHS: return "SINKATTN_BAD_LENGTHS";
+    default: return "SINKATTN_UNKNOWN_STATUS";
+  }
+}
+
+const char* sinkattn_last_error(void) { return g_last_error; }
+
+int sinkattn_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                     int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                     float sm_scale, int32_t causal, int32_t window, void* out, float* lse,
+                     void* stream) {
+  g_last_error[0] = '\0';
+  int rc = check_common(q, k, v, num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window);
+  if (rc) return rc;
+  if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
+  if (!cu_seqlens_q || !cu_seqlens_k) return fail(SINKATTN_INVALID_ARG, "cu_seqlens must be non-null");
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(SINKATTN_INVALID_ARG, "sizes must be non-negative");
+  if (batch > 65535) return fail(SINKATTN_UNSUPPORTED, "batch %d exceeds 65535", batch);
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
+  if (max_seqlen_q > max_seqlen_k)
+    return fail(SINKATTN_INVALID_ARG, "max_seqlen_q (%d) exceeds max_seqlen_k (%d)", max_seqlen_q,
+                max_seqlen_k);
+  if (static_cast<int64_t>(num_kv_heads) * batch * max_seqlen_k >= (int64_t{1} << 31) ||
+      static_cast<int64_t>(total_q) * num_qo_heads >= (int64_t{1} << 31))
+    return fail(SINKATTN_UNSUPPORTED, "problem exceeds 2^31 rows");
+  if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return SINKATTN_OK;
+
+  AttnArgs a{};
+  a.q = q; a.k = k; a.v = v;
+  a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k;
+  a.batch = batch; a.q_len = 0; a.max_q = max_seqlen_q; a.max_kv = max_seqlen_k;
+  a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
+  a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = 1;
+  a.sinks = sinks; a.out = out; a.lse = lse;
+  return launch_attn_mma(a, /*final_mode=*/true, static_cast<cudaStream_t>(stream));
+}
+
+int sinkattn_decode_split(const void* q, const void* k, const void* v,
+                          const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                          int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                          int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
+                          int32_t num_splits, float* part_acc, float* part_md, void* stream) {
+  g_last_error[0] = '\0';
+  int rc = check_common(q, k, v, num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window);
+  if (rc) return rc;
+  if (!kv_indptr) return fail(SINKATTN_INVALID_ARG, "kv_indptr must be non-null");
+  if (!part_acc || !part_md || !aligned16(part_acc) || !aligned16(part_md))
+    return fail(SINKATTN_INVALID_ARG, "partial buffers must be non-null and 16-byte aligned");
+  if (batch < 0 || max_kv_len < 0) return fail(SINKATTN_INVALID_ARG, "sizes must be non-negative");
+  if (batch > 65535) return fail(SINKATTN_UNSUPPORTED, "batch %d exceeds 65535", batch);
+  if (q_len < 1) return fail(SINKATTN_INVALID_ARG, "q_len must be at least 1");
+  if (num_splits < 1) return fail(SINKATTN_INVALID_ARG, "num_splits must be at least 1");
+  if (num_splits > 4096) return fail(SINKATTN_UNSUPPORTED, "num_splits %d exceeds 4096", num_splits);
+  if (q_len > max_kv_len)
+    return fail(SINKATTN_INVALID_ARG, "q_len (%d) exceeds max_kv_len (%d)", q_len, max_kv_len);
+  if (num_qo_heads / num_kv_heads > 64)
+    return fail(SINKATTN_UNSUPPORTED, "GQA group of %d heads exceeds 64", num_qo_heads / num_kv_heads);
+  if (static_cast<int64_t>(num_kv_heads) * batch * max_kv_len >= (int64_t{1} << 31) ||
+      static_cast<int64_t>(batch) * q_len * num_qo_heads * num_splits * head_dim >=
+          (int64_t{1} << 40))
+    return fail(SINKATTN_UNSUPPORTED, "problem too large");
+  if (batch == 0) return SINKATTN_OK;
+
+  AttnArgs a{};
+  a.q = q; a.k = k; a.v = v;
+  a.cu_q = nullptr; a.cu_k = kv_indptr;
+  a.batch = batch; a.q_len = q_len; a.max_q = q_len; a.max_kv = max_kv_len;
+  a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
+  a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = num_splits;
+  a.part_acc = part_acc; a.part_md = part_md;
+  return launch_attn_mma(a, /*final_mode=*/false, static_cast<cudaStream_t>(stream));
+}
+
+int sinkattn_merge(const float* part_acc, const float* part_md, const float* sinks, int32_t rows,
+                   int32_t num_qo_heads, int32_t head_dim, int32_t num_splits, void* out,
+                   float* lse, void* stream) {
+  g_last_error[0] = '\0';
+  if (!part_acc || !part_md || !out)
+    return fail(SINKATTN_INVALID_ARG, "part_acc, part_md and out must be non-null");
+  if (!aligned16(part_acc) || !aligned16(part_md) || !aligned16(out))
+    return fail(SINKATTN_INVALID_ARG, "part_acc, part_md and out must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
+  if (rows < 0 || num_qo_heads <= 0) return fail(SINKATTN_INVALID_ARG, "bad sizes");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(SINKATTN_UNSUPPORTED, "head_dim %d is not 64 or 128", head_dim);
+  if (num_splits < 1) return fail(SINKATTN_INVALID_ARG, "num_splits must be at least 1");
+  return launch_merge(part_acc, part_md, sinks, rows, num_qo_heads, head_dim, num_splits, out,
+                      lse, static_cast<cudaStream_t>(stream));
+}
+
+int sinkattn_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_qo_heads,
+                                    int32_t head_dim, int32_t num_splits, size_t* bytes) {
+  g_last_error[0] = '\0';
+  if (!bytes) return fail(SINKATTN_INVALID_ARG, "bytes must be non-null");
+  if (batch < 0 || q_len < 1 || num_qo_heads <= 0 || num_splits < 1)
+    return fail(SINKATTN_INVALID_ARG, "bad sizes");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(SINKATTN_UNSUPPORTED, "head_dim %d is not 64 or 128", head_dim);
+  const size_t slots = static_cast<size_t>(batch) * q_len * num_qo_heads * num_splits;
+  const size_t acc = (slots * head_dim * 4 + 255) & ~static_cast<size_t>(255);
+  *bytes = acc + slots * 2 * 4;
+  return SINKATTN_OK;
+}
+
+int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, int32_t num_qo_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t max_kv_len,
+                                   int32_t* num_splits) {
+  g_last_error[0] = '\0';
+  if (!num_splits) return fail(SINKATTN_INVALID_ARG, "num_splits must be non-null");
+  if (batch < 0 || q_len < 1 || num_qo_heads <= 0 || num_kv_heads <= 0 || max_kv_len < 0)
+    return fail(SINKATTN_INVALID_ARG, "bad sizes");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(SINKATTN_UNSUPPORTED, "head_dim %d is not 64 or 128", head_dim);
+  // Aim for ~4 work items per SM slot so variable lengths even out, but keep
+  // each chunk at least 4 KV tiles long (shorter chunks mostly cost partials).
+  const int64_t items = static_cast<int64_t>(batch) * num_kv_heads;
+  const int64_t target = 8 * static_cast<int64_t>(sm_count());
+  int64_t s = items > 0 ? (target + items - 1) / items : 1;
+  const int kt = head_dim == 64 ? 64 : 32;
+  const int64_t cap = max_kv_len / (4 * kt);
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  if (s > 64) s = 64;
+  *num_splits = static_cast<int32_t>(s);
+  return SINKATTN_OK;
+}
+
+int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
+                    int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
+                    int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
+                    int32_t window, int32_t num_splits, const float* sinks, void* workspace,
+                    size_t workspace_bytes, void* out, float* lse, void* stream) {
+  g_last_error[0] = '\0';
+  int rc;
+  if (num_splits <= 0) {
+    rc = sinkattn_decode_default_splits(batch, q_len, num_qo_heads, num_kv_heads, head_dim,
+                                        max_kv_len, &num_splits);
+    if (rc) return rc;
+  }
+  size_t need = 0;
+  rc = sinkattn_decode_workspace_bytes(batch, q_len, num_qo_heads, head_dim, num_splits, &need);
+  if (rc) return rc;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SINKATTN_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (workspace_bytes < need)
+    return fail(SINKATTN_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
+  const size_t slots = static_cast<size_t>(batch) * q_len * num_qo_heads * num_splits;
+  float* part_acc = static_cast<float*>(workspace);
+  float* part_md = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            ((slots * head_dim * 4 + 255) & ~static_cast<size_t>(255)));
+  rc = sinkattn_decode_split(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads,
+                             num_kv_heads, head_dim, sm_scale, causal, window, num_splits,
+                             part_acc, part_md, stream);
+  if (rc) return rc;
+  if (batch == 0) return SINKATTN_OK;
+  return sinkattn_merge(part_acc, part_md, sinks, batch * q_len, num_qo_heads, head_dim,
+                        num_splits, out, lse, stream);
+}
+
+int sinkattn_debug_status(void* stream, int* status) {
+  g_last_error[0] = '\0';
+  if (!status) return fail(SINKATTN_INVALID_ARG, "status must be non-null");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int a = 0, m = 0;
+  if (read_status_attn_mma(s, &a) || read_status_merge(s, &m))
+    return fail(SINKATTN_CUDA_ERROR, "reading the device status failed: %s",
+                cudaGetErrorString(cudaGetLastError()));
+  *status = a ? a : m;
+  return SINKATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,488 @@
+// Split-KV decode / MTP attention with a per-head softmax sink, on the
+// warp-level tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+//
+// Decode is bound by HBM bandwidth ("Hosting Qwen on Blackwell", section
+// "Decoders": decoding is memory-bound), so this kernel is built to stream
+// each (sequence, KV head) slab of the HND cache exactly once:
+//
+//  * One CTA = (sequence b, KV head, query block, KV chunk). Its rows are
+//    (query token, head-in-group) pairs packed 16 per warp tile, so one K/V
+//    tile in shared memory serves the whole GQA group and every MTP draft.
+//  * A producer warp streams K and V tiles with TMA (128-byte swizzled boxes)
+//    into an NST-stage mbarrier ring; consumer warps own one 16-row tile each
+//    and split the KV tiles of the chunk round-robin into TG token groups.
+//  * Per tile: S = Q K^T on mma.sync, mask, online softmax (running max and
+//    sum per row, max reduced over the 4-lane quads with warp shuffles),
+//    O += P V with P re-packed to bf16 straight from the S accumulators.
+//  * Tiles are right-aligned to the end of the CTA's key range, so no copy
+//    ever reads past the last key the CTA needs; keys before the range that a
+//    tile covers are masked (and are real data or TMA zero-fill, never NaN).
+//
+// Two output modes ("GPT-OSS on Day 0", section "Kernels for GPT-OSS / Sink
+// attention": online softmax with the running max seeded by the sink, and the
+// sink counted once when the sequence is split):
+//  * split mode: the chunk's (m, d, acc) without the sink, merged later;
+//  * final mode (single pass): m starts at the sink, d at 1, and the kernel
+//    writes out = acc / d and lse = m + ln d.
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sinkattn {
+
+__device__ int g_status_attn_mma;
+
+struct MmaParams {
+  const __nv_bfloat16* q;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int q_len;
+  int Hq, Hkv, G;
+  int QB;          // query tokens per CTA
+  int nqb;         // query blocks per sequence in the grid
+  int num_splits;
+  int max_kv;
+  float sm_scale, scale_log2;
+  int causal, window;
+  const float* sinks;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_acc;
+  float* part_md;
+};
+
+template <int D, int RT, int TG, int KT, int NST>
+struct MmaCfg {
+  static constexpr int NW = RT * TG;               // consumer warps
+  static constexpr int THREADS = (NW + 1) * 32;    // + producer warp
+  static constexpr int NSUB = D / 64;              // 64-column sub-tiles
+  static constexpr int SUB_BYTES = KT * 128;
+  static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int XCHG_FLOATS_PER_LANE = D / 2 + 4;
+  static constexpr int XCHG_BYTES = (TG - 1) * RT * 32 * XCHG_FLOATS_PER_LANE * 4;
+  static constexpr int BAR_BYTES = 2 * NST * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + BAR_BYTES + XCHG_BYTES;
+};
+
+template <int D, int RT, int TG, int KT, int NST, bool FINAL>
+__global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const MmaParams p) {
+  using C = MmaCfg<D, RT, TG, KT, NST>;
+  constexpr int NW = C::NW;
+  constexpr float NEG_INF = kNegInf;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE_BYTES);
+  uint64_t* empty = full + NST;
+  int* abort_flag = reinterpret_cast<int*>(empty + NST);
+  float* xchg = reinterpret_cast<float*>(smem + NST * C::STAGE_BYTES + C::BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int kvh = blockIdx.y;
+  const int S = p.num_splits;
+  const int split = blockIdx.x % S;
+  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / S);   // longest query blocks first
+
+  const int q_start = p.cu_q ? p.cu_q[b] : b * p.q_len;
+  const int Lq = p.cu_q ? p.cu_q[b + 1] - q_start : p.q_len;
+  const int k_start = p.cu_k[b];
+  const int Lk = p.cu_k[b + 1] - k_start;
+  const int q0 = qb * p.QB;
+  if (q0 >= Lq) return;   // uniform over the CTA, before any barrier
+  const int nq = min(p.QB, Lq - q0);
+  if (threadIdx.x == 0 && (Lk < Lq || Lk > p.max_kv || Lq < 0))
+    atomicExch(&g_status_attn_mma, SINKATTN_BAD_LENGTHS);
+
+  // Positions of the CTA's first and last query (queries are the last Lq keys).
+  const int pos0 = Lk - Lq + q0;
+  const int posN = pos0 + nq - 1;
+
+  // Key range [k_lo, k_hi) this CTA must visit.
+  int k_lo = 0, k_hi = Lk;
+  if (!FINAL) {
+    const int c = (Lk + S - 1) / S;
+    k_lo = min(split * c, Lk);
+    k_hi = min(k_lo + c, Lk);
+  }
+  if (p.causal) k_hi = min(k_hi, posN + 1);
+  if (p.window > 0) k_lo = max(k_lo, pos0 - p.window + 1);
+  const int ntiles = (k_hi > k_lo) ? (k_hi - k_lo + KT - 1) / KT : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], RT);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == NW) {
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t policy = policy_evict_first();
+      const int slab = k_start * p.Hkv + kvh * Lk;   // tensor-map row of key 0
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % NST;
+        const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
+        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)) break;
+        uint8_t* kt = tiles + st * C::STAGE_BYTES;
+        uint8_t* vt = kt + C::TILE_BYTES;
+        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+        const int row = slab + k_hi - (ntiles - i) * KT;
+#pragma unroll
+        for (int sub = 0; sub < C::NSUB; ++sub) {
+          tma_load_2d_hint(kt + sub * C::SUB_BYTES, &tmK, sub * 64, row, &full[st], policy);
+          tma_load_2d_hint(vt + sub * C::SUB_BYTES, &tmV, sub * 64, row, &full[st], policy);
+        }
+        issued = i + 1;
+      }
+      if (*abort_flag) {   // let every copy land before the CTA's shared memory goes away
+        for (int i = max(0, issued - NST); i < issued; ++i)
+          mbar_drain(&full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int rt = warp % RT;
+  const int tg = warp / RT;
+  const int G = p.G;
+
+  int pos[2], tok[2], head[2];
+  bool valid[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = rt * 16 + (lane >> 2) + 8 * i;
+    const int tl = r / G;
+    valid[i] = tl < nq;
+    pos[i] = pos0 + tl;
+    tok[i] = q_start + q0 + tl;
+    head[i] = kvh * G + (r - tl * G);
+  }
+
+  // Q fragments (A operand, row-major 16 x 16 per k-step), loaded once.
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+    for (int reg = 0; reg < 4; ++reg) {
+      const int i = reg & 1;
+      const int col = kk * 16 + (lane & 3) * 2 + ((reg >> 1) << 3);
+      qa[kk][reg] = valid[i]
+                        ? *reinterpret_cast<const uint32_t*>(
+                              p.q + (static_cast<size_t>(tok[i]) * p.Hq + head[i]) * D + col)
+                        : 0u;
+    }
+  }
+
+  // Running state per row, in raw logit units (before sm_scale).
+  float m[2], l[2];
+  float o[D / 8][4];
+#pragma unroll
+  for (int jd = 0; jd < D / 8; ++jd) o[jd][0] = o[jd][1] = o[jd][2] = o[jd][3] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    m[i] = NEG_INF;
+    l[i] = 0.f;
+    if (FINAL && tg == 0 && p.sinks != nullptr && valid[i]) {
+      // Seed with the sink: m = s_h, d = 1 (one lane of the quad holds the 1).
+      const float s = p.sinks[head[i]];
+      m[i] = s / p.sm_scale;
+      l[i] = ((lane & 3) == 0 && s != NEG_INF) ? 1.f : 0.f;
+    }
+  }
+
+  const float c2 = p.scale_log2;
+  for (int i = tg; i < ntiles; i += TG) {
+    const int st = i % NST;
+    const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
+    if (!mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma)) break;
+    const uint32_t kbase = smem_u32(tiles + st * C::STAGE_BYTES);
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const int j0 = k_hi - (ntiles - i) * KT;   // key index of tile row 0
+
+    float s[KT / 8][4];
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+
+    // S = Q K^T
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk += 2) {
+#pragma unroll
+      for (int j = 0; j < KT / 8; ++j) {
+        const int trow = 8 * j + (lane & 7);
+        const int chunk = 2 * kk + (lane >> 3);
+        uint32_t bf[4];
+        ldsm_x4(bf, kbase + (chunk >> 3) * C::SUB_BYTES + sw128_offset(trow, chunk & 7));
+        mma_bf16_16816(s[j], qa[kk], bf[0], bf[1]);
+        mma_bf16_16816(s[j], qa[kk + 1], bf[2], bf[3]);
+      }
+    }
+
+    // Mask (skipped for tiles that every row sees whole).
+    const bool whole = (j0 >= k_lo) && (!p.causal || j0 + KT - 1 <= pos0) &&
+                       (p.window <= 0 || j0 > posN - p.window);
+    if (!whole) {
+#pragma unroll
+      for (int j = 0; j < KT / 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = j0 + 8 * j + (lane & 3) * 2 + (e & 1);
+          const int ps = pos[e >> 1];
+          const bool vis = key >= k_lo && (!p.causal || key <= ps) &&
+                           (p.window <= 0 || key > ps - p.window);
+          if (!vis) s[j][e] = NEG_INF;
+        }
+      }
+    }
+
+    // Online softmax.
+    float mx[2] = {m[0], m[1]};
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j) {
+      mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
+      mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
+    }
+    float sc[2], alpha[2];
+#pragma unroll
+    for (int i2 = 0; i2 < 2; ++i2) {
+      mx[i2] = fmaxf(mx[i2], __shfl_xor_sync(0xffffffffu, mx[i2], 1));
+      mx[i2] = fmaxf(mx[i2], __shfl_xor_sync(0xffffffffu, mx[i2], 2));
+      alpha[i2] = (mx[i2] == NEG_INF) ? 1.f : ex2((m[i2] - mx[i2]) * c2);
+      sc[i2] = (mx[i2] == NEG_INF) ? 0.f : mx[i2] * c2;
+      m[i2] = mx[i2];
+    }
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j) {
+      s[j][0] = ex2(fmaf(s[j][0], c2, -sc[0]));
+      s[j][1] = ex2(fmaf(s[j][1], c2, -sc[0]));
+      s[j][2] = ex2(fmaf(s[j][2], c2, -sc[1]));
+      s[j][3] = ex2(fmaf(s[j][3], c2, -sc[1]));
+      rs[0] += s[j][0] + s[j][1];
+      rs[1] += s[j][2] + s[j][3];
+    }
+    l[0] = l[0] * alpha[0] + rs[0];
+    l[1] = l[1] * alpha[1] + rs[1];
+#pragma unroll
+    for (int jd = 0; jd < D / 8; ++jd) {
+      o[jd][0] *= alpha[0];
+      o[jd][1] *= alpha[0];
+      o[jd][2] *= alpha[1];
+      o[jd][3] *= alpha[1];
+    }
+
+    // O += P V
+#pragma unroll
+    for (int kt2 = 0; kt2 < KT / 16; ++kt2) {
+      uint32_t a[4];
+      a[0] = pack_bf16x2(s[2 * kt2][0], s[2 * kt2][1]);
+      a[1] = pack_bf16x2(s[2 * kt2][2], s[2 * kt2][3]);
+      a[2] = pack_bf16x2(s[2 * kt2 + 1][0], s[2 * kt2 + 1][1]);
+      a[3] = pack_bf16x2(s[2 * kt2 + 1][2], s[2 * kt2 + 1][3]);
+#pragma unroll
+      for (int jd = 0; jd < D / 8; jd += 2) {
+        const int mi = lane >> 3;
+        const int trow = 16 * kt2 + (mi & 1) * 8 + (lane & 7);
+        const int chunk = jd + (mi >> 1);
+        uint32_t bf[4];
+        ldsm_x4_trans(bf, vbase + (chunk >> 3) * C::SUB_BYTES + sw128_offset(trow, chunk & 7));
+        mma_bf16_16816(o[jd], a, bf[0], bf[1]);
+        mma_bf16_16816(o[jd + 1], a, bf[2], bf[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // Row sums are split over the 4 lanes of each quad.
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    l[i] += __shfl_xor_sync(0xffffffffu, l[i], 1);
+    l[i] += __shfl_xor_sync(0xffffffffu, l[i], 2);
+  }
+
+  // Combine the token groups of each row tile.
+  if (TG > 1) {
+    if (tg > 0) {
+      float* slot = xchg + ((tg - 1) * RT + rt) * 32 * C::XCHG_FLOATS_PER_LANE +
+                    lane * C::XCHG_FLOATS_PER_LANE;
+#pragma unroll
+      for (int jd = 0; jd < D / 8; ++jd)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) slot[jd * 4 + e] = o[jd][e];
+      slot[D / 2 + 0] = m[0];
+      slot[D / 2 + 1] = m[1];
+      slot[D / 2 + 2] = l[0];
+      slot[D / 2 + 3] = l[1];
+    }
+    named_barrier_sync(1, NW * 32);
+    if (tg > 0) return;
+#pragma unroll 1
+    for (int t = 1; t < TG; ++t) {
+      const float* slot = xchg + ((t - 1) * RT + rt) * 32 * C::XCHG_FLOATS_PER_LANE +
+                          lane * C::XCHG_FLOATS_PER_LANE;
+      float a0[2], a1[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float m2 = slot[D / 2 + i];
+        const float l2 = slot[D / 2 + 2 + i];
+        const float mn = fmaxf(m[i], m2);
+        a0[i] = (m[i] == NEG_INF) ? 0.f : ex2((m[i] - mn) * c2);
+        a1[i] = (m2 == NEG_INF) ? 0.f : ex2((m2 - mn) * c2);
+        l[i] = l[i] * a0[i] + l2 * a1[i];
+        m[i] = mn;
+      }
+#pragma unroll
+      for (int jd = 0; jd < D / 8; ++jd) {
+        o[jd][0] = o[jd][0] * a0[0] + slot[jd * 4 + 0] * a1[0];
+        o[jd][1] = o[jd][1] * a0[0] + slot[jd * 4 + 1] * a1[0];
+        o[jd][2] = o[jd][2] * a0[1] + slot[jd * 4 + 2] * a1[1];
+        o[jd][3] = o[jd][3] * a0[1] + slot[jd * 4 + 3] * a1[1];
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ epilogue
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (!valid[i]) continue;
+    const size_t rowid = static_cast<size_t>(tok[i]) * p.Hq + head[i];
+    if (FINAL) {
+      const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+      __nv_bfloat16* orow = p.out + rowid * D;
+#pragma unroll
+      for (int jd = 0; jd < D / 8; ++jd) {
+        const int col = jd * 8 + (lane & 3) * 2;
+        *reinterpret_cast<uint32_t*>(orow + col) =
+            pack_bf16x2(o[jd][2 * i] * inv, o[jd][2 * i + 1] * inv);
+      }
+      if (p.lse != nullptr && (lane & 3) == 0)
+        p.lse[rowid] = l[i] > 0.f ? (m[i] * c2 + lg2(l[i])) * kLn2 : NEG_INF;
+    } else {
+      float* arow = p.part_acc + (rowid * S + split) * D;
+#pragma unroll
+      for (int jd = 0; jd < D / 8; ++jd) {
+        const int col = jd * 8 + (lane & 3) * 2;
+        *reinterpret_cast<float2*>(arow + col) = make_float2(o[jd][2 * i], o[jd][2 * i + 1]);
+      }
+      if ((lane & 3) == 0) {
+        float2 md;
+        md.x = (m[i] == NEG_INF) ? NEG_INF : m[i] * p.sm_scale;
+        md.y = l[i];
+        *reinterpret_cast<float2*>(p.part_md + (rowid * S + split) * 2) = md;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int D, int RT, int TG, int KT, int NST, bool FINAL>
+static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
+  using C = MmaCfg<D, RT, TG, KT, NST>;
+  CUtensorMap tmK, tmV;
+  const uint64_t rows = static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
+  int rc = make_rows_tmap(&tmK, a.k, rows, D, KT, 128);
+  if (rc) return rc;
+  rc = make_rows_tmap(&tmV, a.v, rows, D, KT, 128);
+  if (rc) return rc;
+
+  MmaParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.q_len = a.q_len;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.Hq / a.Hkv;
+  p.QB = FINAL ? (16 * RT) / p.G : ((a.q_len * p.G <= 16 * RT) ? a.q_len : (16 * RT) / p.G);
+  const int maxq = a.cu_q ? a.max_q : a.q_len;
+  p.nqb = (maxq + p.QB - 1) / p.QB;
+  p.num_splits = FINAL ? 1 : a.num_splits;
+  p.max_kv = a.max_kv;
+  p.sm_scale = a.sm_scale;
+  p.scale_log2 = a.sm_scale * kLog2e;
+  p.causal = a.causal;
+  p.window = a.window;
+  p.sinks = a.sinks;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.part_acc = a.part_acc;
+  p.part_md = a.part_md;
+
+  auto kern = attn_mma_kernel<D, RT, TG, KT, NST, FINAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) {
+    set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    return SINKATTN_CUDA_ERROR;
+  }
+  const dim3 grid(static_cast<unsigned>(p.nqb * p.num_splits), static_cast<unsigned>(a.Hkv),
+                  static_cast<unsigned>(a.batch));
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmK, tmV, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("attention kernel launch: %s", cudaGetErrorString(e));
+    return SINKATTN_CUDA_ERROR;
+  }
+  return SINKATTN_OK;
+}
+
+int launch_attn_mma(const AttnArgs& a, bool final_mode, cudaStream_t stream) {
+  const int G = a.Hq / a.Hkv;
+  if (final_mode) {
+    if (G > 128) {
+      set_error("GQA group of %d query heads exceeds 128 rows per CTA", G);
+      return SINKATTN_UNSUPPORTED;
+    }
+    if (a.d == 64) return launch_cfg<64, 8, 1, 64, 3, true>(a, stream);
+    return launch_cfg<128, 8, 1, 64, 2, true>(a, stream);
+  }
+  const int rows = G * a.q_len;
+  const int rt_needed = (rows + 15) / 16;
+  if (G > 64) {
+    set_error("GQA group of %d query heads exceeds 64 rows per CTA", G);
+    return SINKATTN_UNSUPPORTED;
+  }
+  if (a.d == 64) {
+    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4, false>(a, stream);
+    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4, false>(a, stream);
+    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4, false>(a, stream);
+    return launch_cfg<64, 4, 2, 64, 4, false>(a, stream);
+  }
+  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4, false>(a, stream);
+  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4, false>(a, stream);
+  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4, false>(a, stream);
+  return launch_cfg<128, 4, 2, 32, 4, false>(a, stream);
+}
+
+int read_status_attn_mma(cudaStream_t s, int* status) {
+  int zero = 0;
+  if (cudaMemcpyFromSymbolAsync(status, g_status_attn_mma, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SINKATTN_CUDA_ERROR;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_CUDA_ERROR;
+  if (cudaMemcpyToSymbolAsync(g_status_attn_mma, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                              s) != cudaSuccess)
+    return SINKATTN_CUDA_ERROR;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_CUDA_ERROR;
+  return SINKATTN_OK;
+}
+
+}  // namespace sinkattn

@@ -1,0 +1,59 @@
+// Host-side interface between the C ABI (api.cu) and the kernel translation
+// units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sinkattn {
+
+// Everything the attention kernels need besides the K/V tensor maps.
+struct AttnArgs {
+  const void* q;            // bf16 [total_q, Hq, d]
+  const void* k;            // bf16 ragged HND
+  const void* v;            // bf16 ragged HND
+  const int32_t* cu_q;      // [B+1] (prefill) or nullptr (decode: uniform q_len)
+  const int32_t* cu_k;      // [B+1]
+  int32_t batch, q_len, max_q, max_kv;
+  int32_t Hq, Hkv, d;
+  float sm_scale;
+  int32_t causal, window;
+  int32_t num_splits;       // 1 for the single-pass (final) mode
+  // final mode
+  const float* sinks;
+  void* out;
+  float* lse;
+  // split mode
+  float* part_acc;
+  float* part_md;
+};
+
+// Encodes a 2-D tensor map over a [rows, d] bf16 buffer with [box_rows, 64]
+// boxes and 128-byte swizzling. Returns 0 or a SINKATTN_* status.
+int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
+                   int swizzle_bytes);
+
+// Split-KV (num_splits >= 1, partial outputs) or single-pass (final outputs)
+// attention on the warp-level tensor-core path. Returns a SINKATTN_* status.
+int launch_attn_mma(const AttnArgs& a, bool final_mode, cudaStream_t stream);
+
+// Single-pass prefill on the tcgen05/TMEM path. Returns a SINKATTN_* status.
+int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
+
+int launch_merge(const float* part_acc, const float* part_md, const float* sinks, int32_t rows,
+                 int32_t Hq, int32_t d, int32_t num_splits, void* out, float* lse,
+                 cudaStream_t stream);
+
+// Reads and clears the device status word of one translation unit.
+int read_status_attn_mma(cudaStream_t s, int* status);
+int read_status_merge(cudaStream_t s, int* status);
+int read_status_prefill_tc(cudaStream_t s, int* status);
+
+// Thread-local error text used by the C ABI.
+void set_error(const char* fmt, ...);
+
+// Number of SMs on the current device (queried once).
+int sm_count();
+
+}  // namespace sinkattn

@@ -1,0 +1,176 @@
+/*
+ * sinkattn — grouped-query attention with a learned per-head softmax sink,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("GPT-OSS on Day 0", Perplexity, section "Kernels for GPT-OSS /
+ * Sink attention"; "Attention: GQA with attention sinks"):
+ *
+ *     attn = softmax(q @ k^T * sm_scale + sink) * V
+ *
+ * where the sink s_h of query head h is one extra logit column whose value row
+ * is zero:
+ *
+ *     out_i = sum_j e^{l_j - M} v_j / (e^{s_h - M} + sum_j e^{l_j - M}),
+ *     l_j   = sm_scale * q_i . k_j,   M = max(s_h, max_j l_j),
+ *     lse_i = M + ln(e^{s_h - M} + sum_j e^{l_j - M})      (natural log, sink included).
+ *
+ * Several query heads share one KV head (GQA): query head h reads KV head
+ * floor(h / G), G = num_qo_heads / num_kv_heads. The online softmax seeds its
+ * running max with the head's sink (m = s_h, d = 1), so the sink is counted
+ * exactly once; when the keys are split into chunks (split-KV decode), the
+ * chunks carry no sink and the merge seeds with it (same section: the sink
+ * belongs to one block only).
+ *
+ * Layouts (all device memory, row-major, contiguous):
+ *   q, out       bf16 [total_q, Hq, d]  (token-major). Decode: total_q = batch*q_len,
+ *                token b*q_len + t is draft t of sequence b.
+ *   k, v         bf16 ragged HND ("Hosting Qwen on Blackwell", section "Deployment on
+ *                GB200 NVL72": heads leading, tokens contiguous): sequence b is the
+ *                contiguous block [Hkv, Lk_b, d] starting at element Hkv*cu_k[b]*d.
+ *   sinks        fp32 [Hq], natural-log units of the scaled logits; NULL = no sink.
+ *   lse          fp32 [total_q, Hq]; NULL = not written.
+ *   cu_seqlens_* int32 [batch+1], non-decreasing, cu[0] = 0 (device memory).
+ *
+ * Masking: query i of a sequence with Lq queries and Lk keys sits at position
+ * p = Lk - Lq + i (queries are the last Lq positions). causal: key j visible
+ * iff j <= p. window W > 0 (requires causal): additionally j > p - W, i.e. the
+ * W keys p-W+1 .. p. A row with no visible key and no sink gets out = 0,
+ * lse = -inf; with a sink and no key, out = 0, lse = s_h.
+ *
+ * Supported: head_dim 64 or 128; num_qo_heads % num_kv_heads == 0; sm_scale > 0.
+ *
+ * Ownership and streams: the caller allocates and owns every buffer,
+ * including the decode workspace. The library never allocates, frees or
+ * synchronises in these calls; it enqueues kernels on `stream` (a
+ * cudaStream_t; NULL = legacy default stream) and returns. Inputs are read
+ * only. q, k, v, out and the partial buffers must be 16-byte aligned.
+ *
+ * Errors: every call validates its arguments on the host before launching
+ * anything and returns a status code; on error nothing is launched and
+ * sinkattn_last_error() (thread-local) describes the problem. Faults inside a
+ * kernel (for example a bounded wait that gave up, or device-side lengths
+ * that contradict the host-side sizes) are recorded in a device status word
+ * that sinkattn_debug_status() reads.
+ */
+#ifndef SINKATTN_H_
+#define SINKATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SINKATTN_API __attribute__((visibility("default")))
+#else
+#define SINKATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum sinkattn_status {
+  SINKATTN_OK = 0,
+  SINKATTN_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad workspace */
+  SINKATTN_UNSUPPORTED = 2,  /* head_dim not 64/128, Hq % Hkv != 0, window without causal */
+  SINKATTN_CUDA_ERROR = 3,   /* a CUDA runtime/driver call or launch failed */
+  SINKATTN_TIMEOUT = 4,      /* device status: a bounded wait inside a kernel gave up */
+  SINKATTN_BAD_LENGTHS = 5   /* device status: cu_seqlens/kv_indptr contradict the host sizes */
+};
+
+/*
+ * Prefill / varlen attention with sink, single pass (no split), output
+ * normalised. Steps: logits, mask, online softmax seeded with the sink,
+ * P·V, finalize ("GPT-OSS on Day 0", "Kernels for GPT-OSS / Sink attention").
+ *
+ *   q [total_q, Hq, d], k/v ragged HND, sinks [Hq] or NULL,
+ *   cu_seqlens_q / cu_seqlens_k [batch+1] (device),
+ *   batch, total_q, max_seqlen_q, max_seqlen_k: host-side sizes for the grid
+ *     (max_seqlen_* must bound every sequence; total_q = cu_seqlens_q[batch]),
+ *   causal (0/1), window (<= 0: none; > 0 requires causal),
+ *   out [total_q, Hq, d] bf16, lse [total_q, Hq] fp32 or NULL.
+ * Each sequence needs Lq_b <= Lk_b.
+ */
+SINKATTN_API int sinkattn_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                     int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                     float sm_scale, int32_t causal, int32_t window, void* out, float* lse,
+                     void* stream);
+
+/*
+ * Split-KV decode / MTP, step 1: per-chunk partial state WITHOUT the sink
+ * (heads and KV length both parallel: same section, "parallelise over heads
+ * and KV sequence length").
+ *
+ *   q [batch*q_len, Hq, d] bf16; k/v ragged HND with kv_indptr [batch+1] (device);
+ *   max_kv_len bounds every Lk_b (host); each sequence needs Lk_b >= q_len.
+ *   Sequence b's keys are cut into num_splits chunks of c = ceil(Lk_b/num_splits)
+ *   keys; chunk s covers [s*c, min((s+1)*c, Lk_b)) and may be empty.
+ *   part_acc: fp32 [batch*q_len, Hq, num_splits, d]: sum_j e^{l_j - m_s} v_j;
+ *   part_md:  fp32 [batch*q_len, Hq, num_splits, 2]: (m_s, d_s) with m_s the
+ *             largest visible logit of the chunk (natural units) and
+ *             d_s = sum_j e^{l_j - m_s}; an empty chunk gives (-inf, 0) and acc 0.
+ */
+SINKATTN_API int sinkattn_decode_split(const void* q, const void* k, const void* v,
+                          const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                          int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                          int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
+                          int32_t num_splits, float* part_acc, float* part_md, void* stream);
+
+/*
+ * Split-KV decode / MTP, step 2: fold the num_splits partials of every
+ * (row, head) with the sink counted exactly once: the running state starts at
+ * m = s_h, d = 1 (m = -inf, d = 0 without a sink) and absorbs each chunk with
+ * the rescale to the larger maximum; out = acc / d, lse = m + ln d.
+ *   part_acc/part_md as produced by sinkattn_decode_split; rows = batch*q_len;
+ *   out [rows, Hq, d] bf16; lse [rows, Hq] fp32 or NULL.
+ */
+SINKATTN_API int sinkattn_merge(const float* part_acc, const float* part_md, const float* sinks,
+                   int32_t rows, int32_t num_qo_heads, int32_t head_dim, int32_t num_splits,
+                   void* out, float* lse, void* stream);
+
+/*
+ * Split-KV decode / MTP in one call: sinkattn_decode_split then sinkattn_merge
+ * on the same stream, with the partials in the caller's workspace (at least
+ * sinkattn_decode_workspace_bytes() bytes, 256-byte aligned).
+ * num_splits <= 0 selects sinkattn_decode_default_splits().
+ */
+SINKATTN_API int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
+                    int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
+                    int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
+                    int32_t window, int32_t num_splits, const float* sinks, void* workspace,
+                    size_t workspace_bytes, void* out, float* lse, void* stream);
+
+/* Workspace bytes sinkattn_decode needs for these sizes (host only, no CUDA call). */
+SINKATTN_API int sinkattn_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_qo_heads,
+                                    int32_t head_dim, int32_t num_splits, size_t* bytes);
+
+/*
+ * The split count sinkattn_decode uses when given num_splits <= 0: enough
+ * (sequence, KV head, chunk) work items to fill every SM several times over,
+ * without chunks shorter than a few KV tiles. Host only; queries the current
+ * device's SM count once.
+ */
+SINKATTN_API int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, int32_t num_qo_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t max_kv_len,
+                                   int32_t* num_splits);
+
+/* Human-readable name of a status code (static string). */
+SINKATTN_API const char* sinkattn_status_string(int status);
+
+/* Description of the last error returned on this thread ("" if none). */
+SINKATTN_API const char* sinkattn_last_error(void);
+
+/*
+ * Diagnostic, not for the hot path: synchronises `stream`, then reads and
+ * clears the device status word of every kernel in the library. *status gets
+ * SINKATTN_OK, SINKATTN_TIMEOUT or SINKATTN_BAD_LENGTHS. Returns
+ * SINKATTN_CUDA_ERROR if the synchronisation or the read failed.
+ */
+SINKATTN_API int sinkattn_debug_status(void* stream, int* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINKATTN_H_ */

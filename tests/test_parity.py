@@ -1,0 +1,182 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle,
+element by element, on the same seeded bf16 inputs.
+
+Small shapes span several KV tiles and ragged tails; edge cases cover empty
+sequences, chunked prefill (Lq < Lk), windows of 1, empty KV chunks, sinks of
+-inf / +-30, and peaky logits. Split decode is checked step by step: the
+per-chunk partials against the oracle's partials, the merge on the oracle's
+own partials, and the whole call against the unsplit oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gqa_attention_softmax_gb300 as sa
+from gqa_attention_softmax_gb300 import workloads
+from _helpers import TOL_LSE, TOL_MAX, TOL_MEAN, compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_attention_softmax_gb300 import _build
+    _build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+    yield
+    assert sa.sinkattn_debug_status() == 0
+
+
+def _sinks(kind, Hq, base):
+    if kind == "given":
+        return base
+    if kind == "none":
+        return None
+    if kind == "mixed":
+        vals = [-math.inf, -30.0, -2.0, 0.0, 1.5, 30.0]
+        return torch.tensor([vals[h % len(vals)] for h in range(Hq)], dtype=torch.float32)
+    return torch.full((Hq,), float(kind), dtype=torch.float32)
+
+
+def _run_prefill(inp, Hq, Hkv, d, scale, causal, window, sinks):
+    g = to_dev(inp)
+    s_dev = None if sinks is None else sinks.cuda()
+    out, lse = sa.sinkattn_prefill(g["q"], g["k"], g["v"], s_dev, g["cu_q"], g["cu_k"],
+                                   max(inp["q_lens"]), max(inp["kv_lens"]), Hkv, scale, causal,
+                                   window)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+PREFILL_CASES = [
+    # q_lens, kv_lens, Hq, Hkv, d, causal, window, sinks, q_scale
+    ([130, 1, 67], [130, 1, 67], 8, 1, 64, True, 0, "given", 1.0),
+    ([200, 33], [200, 300], 16, 2, 128, True, 0, "given", 1.0),       # chunked prefill
+    ([129, 64], [129, 64], 64, 4, 128, True, 0, "given", 1.0),         # GQA 16, d 128
+    ([100, 257], [100, 257], 64, 8, 64, True, 128, "given", 1.0),      # window 128
+    ([70], [70], 4, 4, 64, True, 1, "given", 1.0),                     # MHA, window 1
+    ([90, 45], [90, 120], 6, 2, 64, False, 0, "given", 1.0),           # non-causal, G = 3
+    ([0, 50, 0, 3], [10, 50, 0, 3], 8, 2, 64, True, 0, "given", 1.0),  # empty sequences
+    ([96], [96], 8, 1, 128, True, 0, "none", 1.0),
+    ([96], [96], 8, 1, 64, True, 0, "mixed", 1.0),
+    ([150], [150], 16, 1, 64, True, 0, "given", 4.0),                  # peaky logits
+    ([81], [81], 32, 2, 128, True, 17, "mixed", 3.0),
+    ([1, 2, 3], [1, 2, 3], 4, 1, 128, True, 0, "given", 1.0),          # tiny sequences
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=lambda c: "q%s_k%s_h%d-%d_d%d_c%d_w%d_%s_x%g" % (
+    "-".join(map(str, c[0])), "-".join(map(str, c[1])), c[2], c[3], c[4], c[5], c[6], c[7], c[8]))
+def test_prefill_matches_oracle(case):
+    q_lens, kv_lens, Hq, Hkv, d, causal, window, sk, qs = case
+    inp = workloads.explicit_inputs(q_lens, kv_lens, Hq, Hkv, d, seed=21, q_scale=qs)
+    sinks = _sinks(sk, Hq, inp["sinks"])
+    scale = 1.0 / math.sqrt(d)
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], sinks, inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, causal, window)
+    out, lse = _run_prefill(inp, Hq, Hkv, d, scale, causal, window, sinks)
+    compare(out, lse, want_out, want_lse, "prefill")
+
+
+def test_tiny_workload_prefill_and_decode():
+    w = workloads.WORKLOADS["tiny"]
+    inp = workloads.make_inputs(w)
+    Hq, Hkv, d = w.num_qo_heads, w.num_kv_heads, w.head_dim
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, w.scale, True, 0)
+    out, lse = _run_prefill(inp, Hq, Hkv, d, w.scale, True, 0, inp["sinks"])
+    compare(out, lse, want_out, want_lse, "tiny prefill")
+    g = to_dev(inp)
+    for S in (1, 3, 8, 200):
+        out, lse = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], 16, 128, Hkv,
+                                      num_splits=S, sm_scale=w.scale)
+        torch.cuda.synchronize()
+        compare(out, lse, want_out, want_lse, "tiny decode S=%d" % S)
+
+
+def _decode_inputs(B, q_len, Hq, Hkv, d, kv_range, seed, q_scale=1.0):
+    w = workloads.Workload("t", "decode", Hq, Hkv, d, True, batch=B, q_len=q_len,
+                           kv_range=kv_range, sink_dist="uniform2", seed=seed)
+    return workloads.make_inputs(w, q_scale=q_scale)
+
+
+DECODE_CASES = [
+    # B, q_len, Hq, Hkv, d, kv_range, S, window
+    (3, 1, 64, 8, 64, (1, 300), 4, 0),
+    (4, 3, 64, 4, 128, (3, 500), 16, 0),
+    (2, 16, 4, 1, 64, (16, 200), 2, 0),
+    (3, 4, 32, 2, 128, (4, 129), 40, 0),     # more chunks than keys: empty chunks
+    (2, 2, 8, 8, 64, (2, 100), 3, 16),       # window 16
+    (1, 1, 64, 1, 64, (50, 70), 1, 0),       # GQA 64: four warp tiles
+    (2, 5, 16, 1, 128, (5, 90), 2, 0),       # 80 rows: two query blocks
+    (5, 2, 12, 3, 64, (2, 333), 5, 0),       # GQA 4 with odd head count
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: "b%d_q%d_h%d-%d_d%d_k%d-%d_s%d_w%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5][0], c[5][1], c[6], c[7]))
+def test_decode_split_merge_matches_oracle(case):
+    B, q_len, Hq, Hkv, d, kvr, S, window = case
+    inp = _decode_inputs(B, q_len, Hq, Hkv, d, kvr, seed=31 + S)
+    scale = 1.0 / math.sqrt(d)
+    g = to_dev(inp)
+    max_kv = max(inp["kv_lens"])
+
+    # step 1: partials against the oracle's own partials
+    acc, md = sa.sinkattn_decode_split(g["q"], g["k"], g["v"], g["cu_k"], q_len, max_kv, Hkv, S,
+                                       scale, True, window)
+    torch.cuda.synchronize()
+    acc_o, m_o, d_o = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"],
+                                            Hq, Hkv, d, scale, True, window, S)
+    acc_g, md_g = acc.cpu().numpy(), md.cpu().numpy()
+    m_g, d_g = md_g[..., 0], md_g[..., 1]
+    empty = np.isneginf(m_o)
+    assert (np.isneginf(m_g) == empty).all()
+    assert (d_g[empty] == 0).all() and (acc_g[empty] == 0).all()
+    ne = ~empty
+    assert np.abs(m_g[ne] - m_o[ne]).max() <= TOL_LSE
+    assert np.abs(np.log(d_g[ne]) - np.log(d_o[ne])).max() <= TOL_LSE
+    og = acc_g[ne] / d_g[ne][:, None]
+    oo = acc_o[ne] / d_o[ne][:, None]
+    assert np.abs(og - oo).max() <= TOL_MAX and np.abs(og - oo).mean() <= TOL_MEAN
+
+    # step 2: the merge alone, fed the oracle's partials
+    mo, lo = oracle.merge(acc_o, m_o, d_o, inp["sinks"], Hq, d)
+    part_acc = torch.from_numpy(acc_o.astype(np.float32)).cuda()
+    part_md = torch.from_numpy(np.stack([m_o, d_o], -1).astype(np.float32)).cuda()
+    out, lse = sa.sinkattn_merge(part_acc, part_md, g["sinks"])
+    torch.cuda.synchronize()
+    compare(out, lse, mo.reshape(-1, d), lo.reshape(-1), "merge")
+
+    # the whole call against the unsplit oracle
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, True, window)
+    out, lse = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], q_len, max_kv,
+                                  Hkv, num_splits=S, sm_scale=scale, window=window)
+    torch.cuda.synchronize()
+    compare(out, lse, want_out, want_lse, "decode")
+
+
+def test_decode_default_splits_and_no_sink():
+    inp = _decode_inputs(6, 1, 64, 8, 64, (100, 2000), seed=41)
+    g = to_dev(inp)
+    scale = 0.125
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], None, inp["cu_q"], inp["cu_k"],
+                                       64, 8, 64, scale, True, 0)
+    out, lse = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], None, 1,
+                                  max(inp["kv_lens"]), 8, num_splits=0, sm_scale=scale)
+    torch.cuda.synchronize()
+    compare(out, lse, want_out, want_lse, "decode default splits")
+
+
+def test_outputs_are_deterministic():
+    inp = _decode_inputs(4, 3, 64, 4, 128, (200, 900), seed=51)
+    g = to_dev(inp)
+    r1 = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], 3, 900, 4, num_splits=7)
+    r2 = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], 3, 900, 4, num_splits=7)
+    torch.cuda.synchronize()
+    assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
