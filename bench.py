@@ -146,7 +146,7 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         loaded = [s for s, r in zip(sm, rows) if r[3].strip() and float(r[3] or 0) > 0]
         return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
@@ -161,7 +161,8 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False):
     inputs, runner)."""
     from gqa_attention_softmax_gb300 import runner, workloads, _binding as B
     w = workloads.WORKLOADS[name]
-    inp = workloads.make_inputs(w, device="cuda")
+    rank = int(os.environ.get("RANK", "0"))
+    inp = workloads.make_inputs(w, device="cuda", seed=runner.rank_seed(w.seed, rank))
     run = runner.Runner(w, inp)
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -216,12 +217,8 @@ def _sync(ctx):
 
 
 def _max_over_ranks(x, ctx):
-    if ctx is None:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from gqa_attention_softmax_gb300 import runner
+    return runner.max_over_ranks(x)
 
 
 def e2e_decode(w, inp, run, steps):

@@ -48,3 +48,54 @@ class Runner:
         return B.sinkattn_prefill(i["q"], i["k"], i["v"], i["sinks"], i["cu_q"], i["cu_k"],
                                   i["max_q"], i["max_k"], w.num_kv_heads, w.scale, w.causal,
                                   w.window, out=self.out, lse=self.lse, stream=stream)
+
+
+# ----------------------------------------------------------------------------
+# multi-rank host logic (one process per GPU; the path needs no exchange)
+# ----------------------------------------------------------------------------
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank serves its own independent requests: rank r draws its batch
+    with seed base + r (weak scaling, no data-path collective)."""
+    return int(base_seed) + int(rank)
+
+
+def max_over_ranks(x: float) -> float:
+    """Largest value of `x` over all ranks (identity without a process group).
+    Uses a CUDA tensor under NCCL and a CPU tensor under gloo."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_sequences(batch: int, rank: int, world: int) -> range:
+    """Contiguous block of sequence indices owned by `rank` when one batch is
+    split over `world` ranks (sizes differ by at most one)."""
+    base, extra = divmod(batch, world)
+    lo = rank * base + min(rank, extra)
+    return range(lo, lo + base + (1 if rank < extra else 0))
+
+
+def slice_sequences(inp: dict, num_kv_heads: int, seqs) -> dict:
+    """Input set restricted to the sequences `seqs` (contiguous), re-based
+    cu_seqlens; tensors stay on their device."""
+    seqs = list(seqs)
+    cu_q = inp["cu_q"].cpu().tolist()
+    cu_k = inp["cu_k"].cpu().tolist()
+    if not seqs:
+        raise ValueError("empty shard")
+    b0, b1 = seqs[0], seqs[-1] + 1
+    q = inp["q"][cu_q[b0]:cu_q[b1]]
+    k = inp["k"][num_kv_heads * cu_k[b0]:num_kv_heads * cu_k[b1]]
+    v = inp["v"][num_kv_heads * cu_k[b0]:num_kv_heads * cu_k[b1]]
+    dev = inp["q"].device
+    ncq = torch.tensor([c - cu_q[b0] for c in cu_q[b0:b1 + 1]], dtype=torch.int32, device=dev)
+    nck = torch.tensor([c - cu_k[b0] for c in cu_k[b0:b1 + 1]], dtype=torch.int32, device=dev)
+    q_lens = inp["q_lens"][b0:b1]
+    kv_lens = inp["kv_lens"][b0:b1]
+    return dict(q=q, k=k, v=v, sinks=inp["sinks"], cu_q=ncq, cu_k=nck, q_lens=q_lens,
+                kv_lens=kv_lens, batch=b1 - b0, total_q=sum(q_lens), total_k=sum(kv_lens),
+                max_q=max(q_lens), max_k=max(kv_lens))
