@@ -141,6 +141,33 @@ SINKATTN_API int sinkattn_decode(const void* q, const void* k, const void* v, co
                     int32_t window, int32_t num_splits, const float* sinks, void* workspace,
                     size_t workspace_bytes, void* out, float* lse, void* stream);
 
+/*
+ * sinkattn_decode for callers that cannot allocate device memory (for example
+ * code inside another runtime whose memory manager owns all device memory and
+ * gives plugins no allocator, or loops where a cudaMalloc, which may
+ * synchronise the device, is not acceptable). The pages have no counterpart:
+ * this is a deployment convenience, not part of the method.
+ *
+ * Same arguments and results as sinkattn_decode minus the workspace: the
+ * partials live in a fixed 32 MiB array inside the library's own device
+ * memory (every GPU that loads the library holds it until the process exits).
+ * Calls whose partials need more than that (sinkattn_decode_workspace_bytes)
+ * are rejected with SINKATTN_UNSUPPORTED before anything launches. The call
+ * allocates nothing and frees nothing.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. Every call shares the one array: calls whose kernels may overlap on
+ * the GPU (different streams, or several host threads) race on it and must be
+ * serialised by the caller. Nothing needs clearing between calls.
+ */
+SINKATTN_API int sinkattn_decode_noalloc(const void* q, const void* k, const void* v,
+                                         const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                                         int32_t max_kv_len, int32_t num_qo_heads,
+                                         int32_t num_kv_heads, int32_t head_dim, float sm_scale,
+                                         int32_t causal, int32_t window, int32_t num_splits,
+                                         const float* sinks, void* out, float* lse, void* stream);
+
 /* Workspace bytes sinkattn_decode needs for these sizes (host only, no CUDA call). */
 SINKATTN_API int sinkattn_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_qo_heads,
                                     int32_t head_dim, int32_t num_splits, size_t* bytes);
