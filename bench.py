@@ -155,14 +155,14 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
-def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False):
+def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, batch=None):
     """Device time of `steps` passes (events on the launching stream) after
     `warmup` untimed passes. Returns (ms_per_step, split_ms_per_launch or None,
-    inputs, runner)."""
+    inputs, runner). `batch` overrides a decode workload's batch (profiling)."""
     from gqa_attention_softmax_gb300 import runner, workloads, _binding as B
     w = workloads.WORKLOADS[name]
     rank = int(os.environ.get("RANK", "0"))
-    inp = workloads.make_inputs(w, device="cuda", seed=runner.rank_seed(w.seed, rank))
+    inp = workloads.make_inputs(w, device="cuda", seed=runner.rank_seed(w.seed, rank), batch=batch)
     run = runner.Runner(w, inp)
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -387,6 +387,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--profile", metavar="WORKLOAD", default=None,
+                    help="profiling mode: time only this workload (no extras), for ncu")
+    ap.add_argument("--batch", type=int, default=None, help="decode batch override (profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -410,6 +414,17 @@ def main():
     from gqa_attention_softmax_gb300 import workloads
     peaks, peak_src = load_peaks()
 
+    if args.profile:
+        ms, split_ms, w, inp, run = time_workload(args.profile, args.steps, args.warmup, dist_ctx,
+                                                  want_kernel_split=True, batch=args.batch)
+        nb, fl, sb = work(w, inp)
+        if rank == 0:
+            print(json.dumps({"profile": args.profile, "batch": inp["batch"], "ms_per_step": ms,
+                              "split_ms": split_ms, "bytes": nb, "flops": fl,
+                              "GB/s": nb / (ms * 1e-3) / 1e9, "TFLOP/s": fl / (ms * 1e-3) / 1e12}),
+                  flush=True)
+        return
+
     sampler = ClockSampler(local_rank)
     with sampler:
         ms, split_ms, w, inp, run = time_workload(HEADLINE, args.steps, args.warmup, dist_ctx,
@@ -420,9 +435,11 @@ def main():
     split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
     traffic = ncu_traffic("attn_mma_kernel/" + HEADLINE, ["attn_mma.cu", "common.cuh"])
 
-    e2e_ms, h2d, d2h = e2e_decode(w, inp, run, steps=min(args.steps, 20))
-    e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_decode(w, inp, run, steps=min(args.steps, 20))
+        e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     also = []
     if not args.no_also:
