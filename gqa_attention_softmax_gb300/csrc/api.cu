@@ -76,6 +76,29 @@ int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int
   return SINKATTN_OK;
 }
 
+int make_q_tmap(CUtensorMap* map, const void* q, uint64_t total_q, int Hq, int d, int G, int QB) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return SINKATTN_CUDA_ERROR;
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hq),
+                              total_q > 0 ? total_q : 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(Hq) * d * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(QB)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (q) failed (CUresult %d)", static_cast<int>(r));
+    return SINKATTN_CUDA_ERROR;
+  }
+  return SINKATTN_OK;
+}
+
 }  // namespace sinkattn
 
 using namespace sinkattn;
@@ -159,10 +182,13 @@ int sinkattn_prefill(const void* q, const void* k, const void* v, const float* s
   a.q = q; a.k = k; a.v = v;
   a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k;
   a.batch = batch; a.q_len = 0; a.max_q = max_seqlen_q; a.max_kv = max_seqlen_k;
+  a.total_q = total_q;
   a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
   a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = 1;
   a.sinks = sinks; a.out = out; a.lse = lse;
-  return launch_attn_mma(a, /*final_mode=*/true, static_cast<cudaStream_t>(stream));
+  if (num_qo_heads / num_kv_heads > 128)
+    return fail(SINKATTN_UNSUPPORTED, "GQA group of %d heads exceeds 128", num_qo_heads / num_kv_heads);
+  return launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
 }
 
 int sinkattn_decode_split(const void* q, const void* k, const void* v,
@@ -293,11 +319,11 @@ int sinkattn_debug_status(void* stream, int* status) {
   g_last_error[0] = '\0';
   if (!status) return fail(SINKATTN_INVALID_ARG, "status must be non-null");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int a = 0, m = 0;
-  if (read_status_attn_mma(s, &a) || read_status_merge(s, &m))
+  int a = 0, m = 0, t = 0;
+  if (read_status_attn_mma(s, &a) || read_status_merge(s, &m) || read_status_prefill_tc(s, &t))
     return fail(SINKATTN_CUDA_ERROR, "reading the device status failed: %s",
                 cudaGetErrorString(cudaGetLastError()));
-  *status = a ? a : m;
+  *status = a ? a : (t ? t : m);
   return SINKATTN_OK;
 }
 

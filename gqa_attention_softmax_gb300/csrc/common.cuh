@@ -159,6 +159,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Sum of the two bf16 halves of a packed pair, in fp32 (exact widening).
+__device__ __forceinline__ float bf16x2_sum(uint32_t v) {
+  return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
+}
+
 // 2^x on the SFU (MUFU.EX2); exact 0 for -inf.
 __device__ __forceinline__ float ex2(float x) {
   float y;

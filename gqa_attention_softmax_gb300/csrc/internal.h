@@ -16,6 +16,7 @@ struct AttnArgs {
   const int32_t* cu_q;      // [B+1] (prefill) or nullptr (decode: uniform q_len)
   const int32_t* cu_k;      // [B+1]
   int32_t batch, q_len, max_q, max_kv;
+  int32_t total_q;          // rows of q (prefill)
   int32_t Hq, Hkv, d;
   float sm_scale;
   int32_t causal, window;
@@ -33,6 +34,10 @@ struct AttnArgs {
 // boxes and 128-byte swizzling. Returns 0 or a SINKATTN_* status.
 int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
                    int swizzle_bytes);
+
+// Encodes a 3-D tensor map over q [total_q, Hq, d] bf16 whose box is
+// [QB tokens][G heads][64 columns] (128 rows of one GQA group), 128-byte swizzled.
+int make_q_tmap(CUtensorMap* map, const void* q, uint64_t total_q, int Hq, int d, int G, int QB);
 
 // Split-KV (num_splits >= 1, partial outputs) or single-pass (final outputs)
 // attention on the warp-level tensor-core path. Returns a SINKATTN_* status.

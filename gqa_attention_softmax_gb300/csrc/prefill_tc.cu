@@ -1,0 +1,455 @@
+// Varlen prefill with a per-head softmax sink on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+//
+// Prefill is the one dense contraction of the path ("Hosting Qwen on
+// Blackwell", section "Prefillers": prefill is compute-intensive, thousands
+// of tokens processed at once). Per CTA:
+//
+//  * rows: 128 (query token, head-in-group) pairs of one KV head -- QB = 128/G
+//    consecutive tokens times the G query heads sharing that KV head -- so one
+//    K/V tile serves the whole GQA group and the causal diagonal cuts only a
+//    few keys of the last tile (QB tokens wide instead of 128);
+//  * warp 0: TMA producer (Q once as a 3-D box, then K/V tiles of 128 keys
+//    into an NST-stage ring, right-aligned to the end of the key range);
+//  * warp 1: allocates TMEM and issues every MMA from one thread:
+//      S_j = Q K_j^T   (M 128, N 128, K d)  into one of two TMEM S buffers,
+//      O  += P_j V_j   (M 128, N d,   K 128) into the TMEM O accumulator,
+//    in the order S_0, S_1, PV_0, S_2, PV_1, ... so the next S overlaps the
+//    current softmax;
+//  * warps 2-5: softmax, one thread per row (= TMEM lane). The running max
+//    starts at the head's sink and the running sum at 1 ("GPT-OSS on Day 0",
+//    section "Kernels for GPT-OSS / Sink attention"); P_j goes to shared
+//    memory as bf16 in the 128-byte-swizzled K-major layout the MMA reads.
+//    O in TMEM is rescaled (after the previous P.V completes) when a row's
+//    maximum grows; the row sums count the bf16-rounded weights the MMA
+//    applies (for out) and the exact weights (for lse).
+//
+// Every wait is bounded; on a timeout the CTA records SINKATTN_TIMEOUT,
+// drains its copies and MMAs, frees TMEM and exits.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace sinkattn {
+
+__device__ int g_status_prefill_tc;
+
+struct TcParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int Hq, Hkv, G, QB, nqb, max_kv;
+  float sm_scale, scale_log2;
+  int causal, window;
+  const float* sinks;
+  __nv_bfloat16* out;
+  float* lse;
+};
+
+// A row's O and sums are rescaled when its running maximum grows by more than
+// 2^kRescaleLog2. At 0 the maximum is exact, so the largest weight of every
+// row is exactly 1 in bf16; larger values skip rescales at the cost of bf16
+// rounding on weights up to 2^kRescaleLog2.
+constexpr float kRescaleLog2 = 0.f;
+
+template <int D, int NST, int NP>
+struct TcCfg {
+  static constexpr int NSUB = D / 64;
+  static constexpr int KT = 128;                  // keys per tile
+  static constexpr int SUB = 128 * 128;           // [128 rows][64 bf16], 128B-swizzled: 16 KB
+  static constexpr int Q_BYTES = NSUB * SUB;
+  static constexpr int KV_TILE = NSUB * SUB;
+  static constexpr int STAGE = 2 * KV_TILE;       // K and V of one tile
+  static constexpr int P_BYTES = 2 * SUB;         // [128 rows][128 keys] bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + NST * STAGE;
+  static constexpr int OFF_BAR = OFF_P + NP * P_BYTES;
+  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + NP + 1;
+  static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O
+  static constexpr uint32_t COL_O = 256;
+};
+
+template <int D, int NST, int NP>
+__global__ void __launch_bounds__(192, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  using C = TcCfg<D, NST, NP>;
+  constexpr int KT = C::KT;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = q_full + 1;
+  uint64_t* kv_empty = kv_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* drain = pv_done + NP;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* status = &g_status_prefill_tc;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int kvh = blockIdx.y;
+  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x);   // longest query blocks first
+
+  const int q_start = p.cu_q[b];
+  const int Lq = p.cu_q[b + 1] - q_start;
+  const int k_start = p.cu_k[b];
+  const int Lk = p.cu_k[b + 1] - k_start;
+  const int q0 = qb * p.QB;
+  if (q0 >= Lq) return;   // uniform over the CTA, before any barrier or TMEM use
+  const int nq = min(p.QB, Lq - q0);
+  if (threadIdx.x == 0 && (Lk < Lq || Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
+
+  const int pos0 = Lk - Lq + q0;
+  const int posN = pos0 + nq - 1;
+  int k_lo = 0, k_hi = Lk;
+  if (p.causal) k_hi = min(k_hi, posN + 1);
+  if (p.window > 0) k_lo = max(k_lo, pos0 - p.window + 1);
+  const int n = (k_hi > k_lo) ? (k_hi - k_lo + KT - 1) / KT : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+      mbar_init(&p_full[i], 128);
+    }
+    for (int i = 0; i < NP; ++i) mbar_init(&pv_done[i], 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint32_t q_bytes = static_cast<uint32_t>(C::NSUB * 128 * p.G * p.QB);
+      mbar_arrive_expect_tx(q_full, q_bytes);
+#pragma unroll
+      for (int sub = 0; sub < C::NSUB; ++sub)
+        tc::tma_load_3d(smem + C::OFF_Q + sub * C::SUB, &tmQ, sub * 64, kvh * p.G, q_start + q0,
+                        q_full);
+      const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
+      const int slab = k_start * p.Hkv + kvh * Lk;
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % NST;
+        if (!mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1, abort_flag, status)) break;
+        uint8_t* kt = smem + C::OFF_KV + st * C::STAGE;
+        mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+        const int row = slab + k_hi - (n - i) * KT;
+#pragma unroll
+        for (int sub = 0; sub < C::NSUB; ++sub) {
+          tma_load_2d_hint(kt + sub * C::SUB, &tmK, sub * 64, row, &kv_full[st], policy);
+          tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB, &tmV, sub * 64, row, &kv_full[st],
+                           policy);
+        }
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        mbar_drain(q_full, 0);
+        for (int i = max(0, issued - NST); i < issued; ++i)
+          mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
+      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      bool ok = mbar_wait(q_full, 0, abort_flag, status);
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, status)) return false;
+        tc::fence_after_sync();
+        const uint32_t v_base = smem_u32(smem + C::OFF_KV + (i % NST) * C::STAGE + C::KV_TILE);
+        const uint32_t p_base = smem_u32(smem + C::OFF_P + (i % NP) * C::P_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          const uint64_t a = tc::smem_desc_sw128(p_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(v_base + kk * 2048, C::SUB, 1024);
+          tc::mma_ss(tmem + C::COL_O, a, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(&pv_done[i % NP]);
+        tc::commit(&kv_empty[i % NST]);
+        return true;
+      };
+      for (int j = 0; ok && j < n; ++j) {
+        const int st = j % NST;
+        if (!mbar_wait(&kv_full[st], (j / NST) & 1, abort_flag, status)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(&s_free[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, status)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t k_base = smem_u32(smem + C::OFF_KV + st * C::STAGE);
+        const uint32_t d_s = tmem + static_cast<uint32_t>((j & 1) * KT);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = tc::smem_desc_sw128(q_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(k_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
+          tc::mma_ss(d_s, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(&s_full[j & 1]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && n >= 1) ok = issue_pv(n - 1);
+      // every MMA this thread issued has completed before the CTA frees TMEM
+      tc::commit(drain);
+      mbar_drain(drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int G = p.G;
+    const int tl = row / G;
+    const bool valid = tl < nq;
+    const int pos = pos0 + tl;
+    const int h = kvh * G + (row - tl * G);
+    const int tok = q_start + q0 + tl;
+    int lo_r = k_lo, hi_r = k_hi - 1;
+    if (p.window > 0) lo_r = max(lo_r, pos - p.window + 1);
+    if (p.causal) hi_r = min(hi_r, pos);
+    const float c2 = p.scale_log2;
+
+    // l: exact running sum (for lse); lr: sum of the bf16-rounded weights the
+    // P.V MMA applies (for normalising out). Both include the sink's term.
+    float m_used = kNegInf, l = 0.f, lr = 0.f;
+    if (p.sinks != nullptr && valid) {
+      const float s = p.sinks[h];
+      if (s != kNegInf) {
+        m_used = s / p.sm_scale;   // the sink, in raw logit units
+        l = 1.f;
+        lr = 1.f;
+      }
+    }
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    uint8_t* prow = smem + C::OFF_P + row * 128;
+    bool ok = true;
+    // A wait that gives up in any lane makes the whole warp leave, so the
+    // warp-collective TMEM loads/stores below never run with missing lanes.
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+    };
+
+    for (int j = 0; j < n; ++j) {
+      if (!wwait(&s_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+      float s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(lane_addr + (j & 1) * KT + c * 32, s[c]);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      mbar_arrive(&s_free[j & 1]);
+
+      const int j0 = k_hi - (n - j) * KT;
+      if (j0 < lo_r || j0 + KT - 1 > hi_r) {
+        const int clo = lo_r - j0, chi = hi_r - j0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            if (col < clo || col > chi) s[c][e] = kNegInf;
+          }
+      }
+      float mx = kNegInf;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, s[c][e]);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mx > m_used && (m_used == kNegInf || (mx - m_used) * c2 > kRescaleLog2)) {
+        alpha = (m_used == kNegInf) ? 0.f : ex2((m_used - mx) * c2);
+        m_used = mx;
+        rescale = true;
+      }
+      const float mb = (m_used == kNegInf) ? 0.f : m_used * c2;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          s[c][e] = ex2(fmaf(s[c][e], c2, -mb));
+          rs += s[c][e];
+        }
+
+      // P buffer j % NP is free once PV_{j-NP} has completed.
+      if (j >= NP && !wwait(&pv_done[j % NP], ((j - NP) / NP) & 1)) { ok = false; break; }
+      // The row sum is taken over the bf16-rounded P the MMA consumes, so the
+      // final normalisation divides by exactly the weights that were applied.
+      uint8_t* pb = prow + (j % NP) * C::P_BYTES;
+      float rsr = 0.f;
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        const float* v = &s[c16 >> 2][(c16 & 3) * 8];
+        uint4 pk;
+        pk.x = pack_bf16x2(v[0], v[1]);
+        pk.y = pack_bf16x2(v[2], v[3]);
+        pk.z = pack_bf16x2(v[4], v[5]);
+        pk.w = pack_bf16x2(v[6], v[7]);
+        rsr += bf16x2_sum(pk.x) + bf16x2_sum(pk.y) + bf16x2_sum(pk.z) + bf16x2_sum(pk.w);
+        *reinterpret_cast<uint4*>(pb + (c16 >> 3) * C::SUB + (((c16 & 7) ^ (row & 7)) << 4)) = pk;
+      }
+      tc::fence_proxy_async_smem();
+
+      // Rescale O when some row of this warp moved its maximum (warp-uniform).
+      if (__any_sync(0xffffffffu, rescale) && j >= 1) {
+        if (!wwait(&pv_done[(j - 1) % NP], ((j - 1) / NP) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc::tmem_ld32(lane_addr + C::COL_O + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc::tmem_st32(lane_addr + C::COL_O + c * 32, o);
+        }
+        tc::tmem_wait_st();
+      }
+      l = l * alpha + rs;
+      lr = lr * alpha + rsr;
+      tc::fence_before_sync();
+      mbar_arrive(&p_full[j & 1]);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && n >= 1) {
+      ok = wwait(&pv_done[(n - 1) % NP], ((n - 1) / NP) & 1);
+      tc::fence_after_sync();
+    }
+    const float inv = lr > 0.f ? 1.f / lr : 0.f;
+    __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float o[32];
+      if (n >= 1 && ok) {
+        tc::tmem_ld32(lane_addr + C::COL_O + c * 32, o);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      if (valid) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 pk;
+          pk.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+          pk.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+          pk.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+          pk.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+          *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = pk;
+        }
+      }
+    }
+    if (valid && p.lse != nullptr)
+      p.lse[static_cast<size_t>(tok) * p.Hq + h] =
+          l > 0.f ? (m_used * c2 + lg2(l)) * kLn2 : kNegInf;
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D, int NST, int NP>
+static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
+  using C = TcCfg<D, NST, NP>;
+  const int G = a.Hq / a.Hkv;
+  CUtensorMap tmQ, tmK, tmV;
+  const int QB = 128 / G;
+  int rc = make_q_tmap(&tmQ, a.q, static_cast<uint64_t>(a.total_q), a.Hq, D, G, QB);
+  if (rc) return rc;
+  const uint64_t rows = static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
+  rc = make_rows_tmap(&tmK, a.k, rows, D, C::KT, 128);
+  if (rc) return rc;
+  rc = make_rows_tmap(&tmV, a.v, rows, D, C::KT, 128);
+  if (rc) return rc;
+
+  TcParams p{};
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = G;
+  p.QB = QB;
+  p.nqb = (a.max_q + QB - 1) / QB;
+  p.max_kv = a.max_kv;
+  p.sm_scale = a.sm_scale;
+  p.scale_log2 = a.sm_scale * kLog2e;
+  p.causal = a.causal;
+  p.window = a.window;
+  p.sinks = a.sinks;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+
+  auto kern = prefill_tc_kernel<D, NST, NP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) {
+    set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    return SINKATTN_CUDA_ERROR;
+  }
+  const dim3 grid(static_cast<unsigned>(p.nqb), static_cast<unsigned>(a.Hkv),
+                  static_cast<unsigned>(a.batch));
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmQ, tmK, tmV, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("prefill kernel launch: %s", cudaGetErrorString(e));
+    return SINKATTN_CUDA_ERROR;
+  }
+  return SINKATTN_OK;
+}
+
+int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
+  const int G = a.Hq / a.Hkv;
+  if (G > 128) {
+    set_error("GQA group of %d query heads exceeds the 128 rows of a tile", G);
+    return SINKATTN_UNSUPPORTED;
+  }
+  if (a.d == 64) return launch_tc<64, 3, 2>(a, stream);
+  return launch_tc<128, 2, 1>(a, stream);
+}
+
+int read_status_prefill_tc(cudaStream_t s, int* status) {
+  int zero = 0;
+  if (cudaMemcpyFromSymbolAsync(status, g_status_prefill_tc, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SINKATTN_CUDA_ERROR;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_CUDA_ERROR;
+  if (cudaMemcpyToSymbolAsync(g_status_prefill_tc, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                              s) != cudaSuccess)
+    return SINKATTN_CUDA_ERROR;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SINKATTN_CUDA_ERROR;
+  return SINKATTN_OK;
+}
+
+}  // namespace sinkattn
