@@ -224,7 +224,7 @@ int sinkattn_decode_split(const void* q, const void* k, const void* v,
   a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
   a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = num_splits;
   a.part_acc = part_acc; a.part_md = part_md;
-  return launch_attn_mma(a, /*final_mode=*/false, static_cast<cudaStream_t>(stream));
+  return launch_attn_mma(a, static_cast<cudaStream_t>(stream));
 }
 
 int sinkattn_merge(const float* part_acc, const float* part_md, const float* sinks, int32_t rows,

@@ -18,12 +18,10 @@
 //    ever reads past the last key the CTA needs; keys before the range that a
 //    tile covers are masked (and are real data or TMA zero-fill, never NaN).
 //
-// Two output modes ("GPT-OSS on Day 0", section "Kernels for GPT-OSS / Sink
-// attention": online softmax with the running max seeded by the sink, and the
-// sink counted once when the sequence is split):
-//  * split mode: the chunk's (m, d, acc) without the sink, merged later;
-//  * final mode (single pass): m starts at the sink, d at 1, and the kernel
-//    writes out = acc / d and lse = m + ln d.
+// Output: the chunk's (m, d, acc) WITHOUT the sink; the merge kernel seeds
+// with the sink so it counts exactly once ("GPT-OSS on Day 0", section
+// "Kernels for GPT-OSS / Sink attention": online softmax with a running max,
+// the sink in one block only when the sequence is split).
 #include <cstdio>
 
 #include "common.cuh"
@@ -45,9 +43,6 @@ struct MmaParams {
   int max_kv;
   float sm_scale, scale_log2;
   int causal, window;
-  const float* sinks;
-  __nv_bfloat16* out;
-  float* lse;
   float* part_acc;
   float* part_md;
 };
@@ -66,7 +61,7 @@ struct MmaCfg {
   static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + BAR_BYTES + XCHG_BYTES;
 };
 
-template <int D, int RT, int TG, int KT, int NST, bool FINAL>
+template <int D, int RT, int TG, int KT, int NST>
 __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const MmaParams p) {
@@ -106,12 +101,9 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
   const int posN = pos0 + nq - 1;
 
   // Key range [k_lo, k_hi) this CTA must visit.
-  int k_lo = 0, k_hi = Lk;
-  if (!FINAL) {
-    const int c = (Lk + S - 1) / S;
-    k_lo = min(split * c, Lk);
-    k_hi = min(k_lo + c, Lk);
-  }
+  const int chunk = (Lk + S - 1) / S;
+  int k_lo = min(split * chunk, Lk);
+  int k_hi = min(k_lo + chunk, Lk);
   if (p.causal) k_hi = min(k_hi, posN + 1);
   if (p.window > 0) k_lo = max(k_lo, pos0 - p.window + 1);
   const int ntiles = (k_hi > k_lo) ? (k_hi - k_lo + KT - 1) / KT : 0;
@@ -198,12 +190,6 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
   for (int i = 0; i < 2; ++i) {
     m[i] = NEG_INF;
     l[i] = 0.f;
-    if (FINAL && tg == 0 && p.sinks != nullptr && valid[i]) {
-      // Seed with the sink: m = s_h, d = 1 (one lane of the quad holds the 1).
-      const float s = p.sinks[head[i]];
-      m[i] = s / p.sm_scale;
-      l[i] = ((lane & 3) == 0 && s != NEG_INF) ? 1.f : 0.f;
-    }
   }
 
   const float c2 = p.scale_log2;
@@ -362,18 +348,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
   for (int i = 0; i < 2; ++i) {
     if (!valid[i]) continue;
     const size_t rowid = static_cast<size_t>(tok[i]) * p.Hq + head[i];
-    if (FINAL) {
-      const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
-      __nv_bfloat16* orow = p.out + rowid * D;
-#pragma unroll
-      for (int jd = 0; jd < D / 8; ++jd) {
-        const int col = jd * 8 + (lane & 3) * 2;
-        *reinterpret_cast<uint32_t*>(orow + col) =
-            pack_bf16x2(o[jd][2 * i] * inv, o[jd][2 * i + 1] * inv);
-      }
-      if (p.lse != nullptr && (lane & 3) == 0)
-        p.lse[rowid] = l[i] > 0.f ? (m[i] * c2 + lg2(l[i])) * kLn2 : NEG_INF;
-    } else {
+    {
       float* arow = p.part_acc + (rowid * S + split) * D;
 #pragma unroll
       for (int jd = 0; jd < D / 8; ++jd) {
@@ -393,7 +368,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int D, int RT, int TG, int KT, int NST, bool FINAL>
+template <int D, int RT, int TG, int KT, int NST>
 static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   using C = MmaCfg<D, RT, TG, KT, NST>;
   CUtensorMap tmK, tmV;
@@ -411,22 +386,19 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.G = a.Hq / a.Hkv;
-  p.QB = FINAL ? (16 * RT) / p.G : ((a.q_len * p.G <= 16 * RT) ? a.q_len : (16 * RT) / p.G);
+  p.QB = (a.q_len * p.G <= 16 * RT) ? a.q_len : (16 * RT) / p.G;
   const int maxq = a.cu_q ? a.max_q : a.q_len;
   p.nqb = (maxq + p.QB - 1) / p.QB;
-  p.num_splits = FINAL ? 1 : a.num_splits;
+  p.num_splits = a.num_splits;
   p.max_kv = a.max_kv;
   p.sm_scale = a.sm_scale;
   p.scale_log2 = a.sm_scale * kLog2e;
   p.causal = a.causal;
   p.window = a.window;
-  p.sinks = a.sinks;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
-  p.lse = a.lse;
   p.part_acc = a.part_acc;
   p.part_md = a.part_md;
 
-  auto kern = attn_mma_kernel<D, RT, TG, KT, NST, FINAL>;
+  auto kern = attn_mma_kernel<D, RT, TG, KT, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) {
@@ -444,16 +416,8 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   return SINKATTN_OK;
 }
 
-int launch_attn_mma(const AttnArgs& a, bool final_mode, cudaStream_t stream) {
+int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
-  if (final_mode) {
-    if (G > 128) {
-      set_error("GQA group of %d query heads exceeds 128 rows per CTA", G);
-      return SINKATTN_UNSUPPORTED;
-    }
-    if (a.d == 64) return launch_cfg<64, 8, 1, 64, 3, true>(a, stream);
-    return launch_cfg<128, 8, 1, 64, 2, true>(a, stream);
-  }
   const int rows = G * a.q_len;
   const int rt_needed = (rows + 15) / 16;
   if (G > 64) {
@@ -461,15 +425,15 @@ int launch_attn_mma(const AttnArgs& a, bool final_mode, cudaStream_t stream) {
     return SINKATTN_UNSUPPORTED;
   }
   if (a.d == 64) {
-    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4, false>(a, stream);
-    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4, false>(a, stream);
-    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4, false>(a, stream);
-    return launch_cfg<64, 4, 2, 64, 4, false>(a, stream);
+    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4>(a, stream);
+    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4>(a, stream);
+    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4>(a, stream);
+    return launch_cfg<64, 4, 2, 64, 4>(a, stream);
   }
-  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4, false>(a, stream);
-  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4, false>(a, stream);
-  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4, false>(a, stream);
-  return launch_cfg<128, 4, 2, 32, 4, false>(a, stream);
+  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4>(a, stream);
+  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4>(a, stream);
+  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4>(a, stream);
+  return launch_cfg<128, 4, 2, 32, 4>(a, stream);
 }
 
 int read_status_attn_mma(cudaStream_t s, int* status) {

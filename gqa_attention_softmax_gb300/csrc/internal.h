@@ -39,9 +39,9 @@ int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int
 // [QB tokens][G heads][64 columns] (128 rows of one GQA group), 128-byte swizzled.
 int make_q_tmap(CUtensorMap* map, const void* q, uint64_t total_q, int Hq, int d, int G, int QB);
 
-// Split-KV (num_splits >= 1, partial outputs) or single-pass (final outputs)
-// attention on the warp-level tensor-core path. Returns a SINKATTN_* status.
-int launch_attn_mma(const AttnArgs& a, bool final_mode, cudaStream_t stream);
+// Split-KV decode (per-chunk partial outputs) on the warp-level tensor-core
+// path. Returns a SINKATTN_* status.
+int launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 
 // Single-pass prefill on the tcgen05/TMEM path. Returns a SINKATTN_* status.
 int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
