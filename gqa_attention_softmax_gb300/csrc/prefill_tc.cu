@@ -1,28 +1,33 @@
 // Varlen prefill with a per-head softmax sink on the 5th-generation tensor
-// cores (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+// cores (tcgen05.mma, accumulators and P in TMEM, operands staged by TMA).
 //
 // Prefill is the one dense contraction of the path ("Hosting Qwen on
 // Blackwell", section "Prefillers": prefill is compute-intensive, thousands
 // of tokens processed at once). Per CTA:
 //
-//  * rows: 128 (query token, head-in-group) pairs of one KV head -- QB = 128/G
-//    consecutive tokens times the G query heads sharing that KV head -- so one
-//    K/V tile serves the whole GQA group and the causal diagonal cuts only a
-//    few keys of the last tile (QB tokens wide instead of 128);
-//  * warp 0: TMA producer (Q once as a 3-D box, then K/V tiles of 128 keys
-//    into an NST-stage ring, right-aligned to the end of the key range);
-//  * warp 1: allocates TMEM and issues every MMA from one thread:
-//      S_j = Q K_j^T   (M 128, N 128, K d)  into one of two TMEM S buffers,
-//      O  += P_j V_j   (M 128, N d,   K 128) into the TMEM O accumulator,
-//    in the order S_0, S_1, PV_0, S_2, PV_1, ... so the next S overlaps the
-//    current softmax;
-//  * warps 2-5: softmax, one thread per row (= TMEM lane). The running max
-//    starts at the head's sink and the running sum at 1 ("GPT-OSS on Day 0",
-//    section "Kernels for GPT-OSS / Sink attention"); P_j goes to shared
-//    memory as bf16 in the 128-byte-swizzled K-major layout the MMA reads.
-//    O in TMEM is rescaled (after the previous P.V completes) when a row's
-//    maximum grows; the row sums count the bf16-rounded weights the MMA
-//    applies (for out) and the exact weights (for lse).
+//  * rows: two tiles (A, B) of 128 (query token, head-in-group) pairs of one
+//    KV head -- each tile is QB = 128/G consecutive tokens times the G query
+//    heads sharing that KV head -- so one K/V tile in shared memory serves
+//    both tiles and the whole GQA group, and the causal diagonal cuts only a
+//    few keys of the last KV tile;
+//  * warp 0: TMA producer (Q_A and Q_B once as 3-D boxes, then K/V tiles of
+//    128 keys into an NST-stage ring, right-aligned to the end of the key
+//    range so no copy reads past the last key needed);
+//  * warp 1: allocates TMEM and issues every MMA from one thread, ping-ponging
+//    the two tiles so the tensor core works on one while the other's softmax
+//    runs:  S_A(0), S_B(0), then per KV tile j:
+//           PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//    with S_t = Q_t K^T (M 128, N 128, K d; both operands in shared memory)
+//    and O_t += P_t V (M 128, N d, K 128; P_t read from TMEM, V from shared);
+//  * warps 2-5 / 6-9: softmax of tile A / B, one thread per row (= TMEM
+//    lane). The running max starts at the head's sink and the running sum at
+//    1 ("GPT-OSS on Day 0", section "Kernels for GPT-OSS / Sink attention").
+//    Pass 1 streams the row of S from TMEM for its maximum; pass 2 streams it
+//    again, exponentiates, and writes P as bf16 into the first 64 columns of
+//    the same TMEM region (so few registers are live). O_t is rescaled in
+//    TMEM when a row's maximum grows; the previous PV_t has completed by then,
+//    because S_t(j) is only issued after it. Row sums are kept both exact (for
+//    lse) and over the bf16-rounded weights the MMA applies (for out).
 //
 // Every wait is bounded; on a timeout the CTA records SINKATTN_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
@@ -45,38 +50,32 @@ struct TcParams {
   float* lse;
 };
 
-// A row's O and sums are rescaled when its running maximum grows by more than
-// 2^kRescaleLog2. At 0 the maximum is exact, so the largest weight of every
-// row is exactly 1 in bf16; larger values skip rescales at the cost of bf16
-// rounding on weights up to 2^kRescaleLog2.
-constexpr float kRescaleLog2 = 0.f;
-
-template <int D, int NST, int NP>
+template <int D, int NST>
 struct TcCfg {
   static constexpr int NSUB = D / 64;
-  static constexpr int KT = 128;                  // keys per tile
+  static constexpr int KT = 128;                  // keys per KV tile
   static constexpr int SUB = 128 * 128;           // [128 rows][64 bf16], 128B-swizzled: 16 KB
-  static constexpr int Q_BYTES = NSUB * SUB;
+  static constexpr int Q_TILE = NSUB * SUB;
   static constexpr int KV_TILE = NSUB * SUB;
-  static constexpr int STAGE = 2 * KV_TILE;       // K and V of one tile
-  static constexpr int P_BYTES = 2 * SUB;         // [128 rows][128 keys] bf16
+  static constexpr int STAGE = 2 * KV_TILE;       // K and V of one KV tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + NST * STAGE;
-  static constexpr int OFF_BAR = OFF_P + NP * P_BYTES;
-  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + NP + 1;
+  static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
+  static constexpr int OFF_BAR = OFF_KV + NST * STAGE;
+  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
-  static constexpr int THREADS = 192;
-  static constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O
-  static constexpr uint32_t COL_O = 256;
+  static constexpr int THREADS = 320;             // TMA, MMA, 2 x 4 softmax warps
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM columns: S_t (P_t in its first 64 columns) at 128 t, O_t at 256 + D t.
+  static constexpr uint32_t col_s(int t) { return 128u * t; }
+  static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
 };
 
-template <int D, int NST, int NP>
-__global__ void __launch_bounds__(192, 1)
+template <int D, int NST>
+__global__ void __launch_bounds__(320, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
-  using C = TcCfg<D, NST, NP>;
+  using C = TcCfg<D, NST>;
   constexpr int KT = C::KT;
 
   extern __shared__ uint8_t smem_raw[];
@@ -86,11 +85,10 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = q_full + 1;
   uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* drain = pv_done + NP;
+  uint64_t* s_full = kv_empty + NST;   // [2]: S_t(j) written
+  uint64_t* p_full = s_full + 2;       // [2]: P_t(j) written and O_t rescaled (128 arrivals)
+  uint64_t* pv_done = p_full + 2;      // [2]: PV_t(j) completed
+  uint64_t* drain = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* status = &g_status_prefill_tc;
@@ -105,9 +103,9 @@ __global__ void __launch_bounds__(192, 1)
   const int Lq = p.cu_q[b + 1] - q_start;
   const int k_start = p.cu_k[b];
   const int Lk = p.cu_k[b + 1] - k_start;
-  const int q0 = qb * p.QB;
-  if (q0 >= Lq) return;   // uniform over the CTA, before any barrier or TMEM use
-  const int nq = min(p.QB, Lq - q0);
+  const int q0 = qb * 2 * p.QB;   // first token of tile A
+  if (q0 >= Lq) return;           // uniform over the CTA, before any barrier or TMEM use
+  const int nq = min(2 * p.QB, Lq - q0);
   if (threadIdx.x == 0 && (Lk < Lq || Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
 
   const int pos0 = Lk - Lq + q0;
@@ -123,12 +121,11 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&pv_done[t], 1);
     }
-    for (int i = 0; i < NP; ++i) mbar_init(&pv_done[i], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -148,12 +145,14 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const uint32_t q_bytes = static_cast<uint32_t>(C::NSUB * 128 * p.G * p.QB);
+      const uint32_t q_bytes = static_cast<uint32_t>(2 * C::NSUB * 128 * p.G * p.QB);
       mbar_arrive_expect_tx(q_full, q_bytes);
 #pragma unroll
-      for (int sub = 0; sub < C::NSUB; ++sub)
-        tc::tma_load_3d(smem + C::OFF_Q + sub * C::SUB, &tmQ, sub * 64, kvh * p.G, q_start + q0,
-                        q_full);
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int sub = 0; sub < C::NSUB; ++sub)
+          tc::tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + sub * C::SUB, &tmQ, sub * 64,
+                          kvh * p.G, q_start + q0 + t * p.QB, q_full);
       const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
       const int slab = k_start * p.Hkv + kvh * Lk;
       int issued = 0;
@@ -183,52 +182,66 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-      bool ok = mbar_wait(q_full, 0, abort_flag, status);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, status)) return false;
-        tc::fence_after_sync();
-        const uint32_t v_base = smem_u32(smem + C::OFF_KV + (i % NST) * C::STAGE + C::KV_TILE);
-        const uint32_t p_base = smem_u32(smem + C::OFF_P + (i % NP) * C::P_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          const uint64_t a = tc::smem_desc_sw128(p_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(v_base + kk * 2048, C::SUB, 1024);
-          tc::mma_ss(tmem + C::COL_O, a, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc::commit(&pv_done[i % NP]);
-        tc::commit(&kv_empty[i % NST]);
-        return true;
-      };
-      for (int j = 0; ok && j < n; ++j) {
-        const int st = j % NST;
-        if (!mbar_wait(&kv_full[st], (j / NST) & 1, abort_flag, status)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&s_free[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, status)) { ok = false; break; }
-        tc::fence_after_sync();
-        const uint32_t k_base = smem_u32(smem + C::OFF_KV + st * C::STAGE);
-        const uint32_t d_s = tmem + static_cast<uint32_t>((j & 1) * KT);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t k_base = smem_u32(smem + C::OFF_KV + (j % NST) * C::STAGE);
+        const uint32_t qt = q_base + t * C::Q_TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = tc::smem_desc_sw128(q_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
+          const uint64_t a = tc::smem_desc_sw128(qt + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = tc::smem_desc_sw128(k_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
-          tc::mma_ss(d_s, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + C::col_s(t), a, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc::commit(&s_full[j & 1]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        tc::commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_base = smem_u32(smem + C::OFF_KV + (j % NST) * C::STAGE + C::KV_TILE);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          const uint64_t bd = tc::smem_desc_sw128(v_base + kk * 2048, C::SUB, 1024);
+          tc::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, bd, idesc_o,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(&pv_done[t]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, status);
+      if (ok && n > 0) {
+        ok = mbar_wait(&kv_full[0], 0, abort_flag, status);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_s(0, 0);
+          issue_s(1, 0);
+        }
       }
-      if (ok && n >= 1) ok = issue_pv(n - 1);
+      for (int j = 0; ok && j < n; ++j) {
+        for (int t = 0; t < 2; ++t) {
+          if (!mbar_wait(&p_full[t], j & 1, abort_flag, status)) { ok = false; break; }
+          tc::fence_after_sync();
+          issue_pv(t, j);
+          if (t == 1) tc::commit(&kv_empty[j % NST]);
+          if (j + 1 < n) {
+            if (t == 0 && !mbar_wait(&kv_full[(j + 1) % NST], ((j + 1) / NST) & 1, abort_flag, status)) { ok = false; break; }
+            // S_t(j+1) overwrites P_t(j): wait until PV_t(j) has read it.
+            if (!mbar_wait(&pv_done[t], j & 1, abort_flag, status)) { ok = false; break; }
+            tc::fence_after_sync();
+            issue_s(t, j + 1);
+          }
+        }
+      }
       // every MMA this thread issued has completed before the CTA frees TMEM
       tc::commit(drain);
       mbar_drain(drain, 0);
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    const int quad = warp & 3;
+    const int t = (warp - 2) >> 2;   // tile
+    const int quad = warp & 3;       // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const int G = p.G;
-    const int tl = row / G;
-    const bool valid = tl < nq;
+    const int rg = row / G;          // token within the tile
+    const int tl = t * p.QB + rg;    // token within the CTA
+    const bool valid = rg < p.QB && tl < nq;
     const int pos = pos0 + tl;
-    const int h = kvh * G + (row - tl * G);
+    const int h = kvh * G + (row - rg * G);
     const int tok = q_start + q0 + tl;
     int lo_r = k_lo, hi_r = k_hi - 1;
     if (p.window > 0) lo_r = max(lo_r, pos - p.window + 1);
@@ -246,8 +259,9 @@ __global__ void __launch_bounds__(192, 1)
         lr = 1.f;
       }
     }
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    uint8_t* prow = smem + C::OFF_P + row * 128;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t s_addr = lane_base + C::col_s(t);
+    const uint32_t o_addr = lane_base + C::col_o(t);
     bool ok = true;
     // A wait that gives up in any lane makes the whole warp leave, so the
     // warp-collective TMEM loads/stores below never run with missing lanes.
@@ -256,91 +270,88 @@ __global__ void __launch_bounds__(192, 1)
     };
 
     for (int j = 0; j < n; ++j) {
-      if (!wwait(&s_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+      if (!wwait(&s_full[t], j & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      float s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(lane_addr + (j & 1) * KT + c * 32, s[c]);
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      mbar_arrive(&s_free[j & 1]);
-
       const int j0 = k_hi - (n - j) * KT;
-      if (j0 < lo_r || j0 + KT - 1 > hi_r) {
-        const int clo = lo_r - j0, chi = hi_r - j0;
+      const bool masked = (j0 < lo_r || j0 + KT - 1 > hi_r);
+      const int clo = lo_r - j0, chi = hi_r - j0;
+
+      // pass 1: row maximum
+      float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(s_addr + c * 32, v);
+        tc::tmem_wait_ld();
+        if (masked) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = c * 32 + e;
-            if (col < clo || col > chi) s[c][e] = kNegInf;
-          }
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < clo || c * 32 + e > chi) v[e] = kNegInf;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], v[e]);
       }
-      float mx = kNegInf;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, s[c][e]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       float alpha = 1.f;
       bool rescale = false;
-      if (mx > m_used && (m_used == kNegInf || (mx - m_used) * c2 > kRescaleLog2)) {
+      if (mx > m_used) {
         alpha = (m_used == kNegInf) ? 0.f : ex2((m_used - mx) * c2);
         m_used = mx;
         rescale = true;
       }
       const float mb = (m_used == kNegInf) ? 0.f : m_used * c2;
-      float rs = 0.f;
+
+      // pass 2: P = 2^(s*c2 - mb) as bf16 into the first 64 columns of S_t.
+      // Chunk c's 16 packed columns only cover S columns already read.
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(s_addr + c * 32, v);
+        tc::tmem_wait_ld();
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          s[c][e] = ex2(fmaf(s[c][e], c2, -mb));
-          rs += s[c][e];
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < clo || c * 32 + e > chi) v[e] = kNegInf;
         }
-
-      // P buffer j % NP is free once PV_{j-NP} has completed.
-      if (j >= NP && !wwait(&pv_done[j % NP], ((j - NP) / NP) & 1)) { ok = false; break; }
-      // The row sum is taken over the bf16-rounded P the MMA consumes, so the
-      // final normalisation divides by exactly the weights that were applied.
-      uint8_t* pb = prow + (j % NP) * C::P_BYTES;
-      float rsr = 0.f;
+        uint32_t pk[16];
 #pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        const float* v = &s[c16 >> 2][(c16 & 3) * 8];
-        uint4 pk;
-        pk.x = pack_bf16x2(v[0], v[1]);
-        pk.y = pack_bf16x2(v[2], v[3]);
-        pk.z = pack_bf16x2(v[4], v[5]);
-        pk.w = pack_bf16x2(v[6], v[7]);
-        rsr += bf16x2_sum(pk.x) + bf16x2_sum(pk.y) + bf16x2_sum(pk.z) + bf16x2_sum(pk.w);
-        *reinterpret_cast<uint4*>(pb + (c16 >> 3) * C::SUB + (((c16 & 7) ^ (row & 7)) << 4)) = pk;
+        for (int e = 0; e < 32; e += 2) {
+          const float a0 = ex2(fmaf(v[e], c2, -mb));
+          const float a1 = ex2(fmaf(v[e + 1], c2, -mb));
+          rs4[(e >> 1) & 3] += a0 + a1;
+          pk[e >> 1] = pack_bf16x2(a0, a1);
+          rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+        }
+        tc::tmem_st16(s_addr + c * 16, pk);
       }
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
 
-      // Rescale O when some row of this warp moved its maximum (warp-uniform).
-      if (__any_sync(0xffffffffu, rescale) && j >= 1) {
-        if (!wwait(&pv_done[(j - 1) % NP], ((j - 1) / NP) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
+      // Rescale O_t when some row of this warp moved its maximum (warp-uniform).
+      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tc::tmem_ld32(lane_addr + C::COL_O + c * 32, o);
+          tc::tmem_ld32(o_addr + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc::tmem_st32(lane_addr + C::COL_O + c * 32, o);
+          tc::tmem_st32(o_addr + c * 32, o);
         }
         tc::tmem_wait_st();
       }
       l = l * alpha + rs;
-      lr = lr * alpha + rsr;
+      lr = lr * alpha + rr;
       tc::fence_before_sync();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive(&p_full[t]);
     }
 
     // ------------------------------------------------------------ epilogue
     if (ok && n >= 1) {
-      ok = wwait(&pv_done[(n - 1) % NP], ((n - 1) / NP) & 1);
+      ok = wwait(&pv_done[t], (n - 1) & 1);
       tc::fence_after_sync();
     }
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int c = 0; c < D / 32; ++c) {
       float o[32];
       if (n >= 1 && ok) {
-        tc::tmem_ld32(lane_addr + C::COL_O + c * 32, o);
+        tc::tmem_ld32(o_addr + c * 32, o);
         tc::tmem_wait_ld();
       } else {
 #pragma unroll
@@ -381,9 +392,9 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int D, int NST, int NP>
+template <int D, int NST>
 static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
-  using C = TcCfg<D, NST, NP>;
+  using C = TcCfg<D, NST>;
   const int G = a.Hq / a.Hkv;
   CUtensorMap tmQ, tmK, tmV;
   const int QB = 128 / G;
@@ -402,7 +413,7 @@ static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
   p.Hkv = a.Hkv;
   p.G = G;
   p.QB = QB;
-  p.nqb = (a.max_q + QB - 1) / QB;
+  p.nqb = (a.max_q + 2 * QB - 1) / (2 * QB);
   p.max_kv = a.max_kv;
   p.sm_scale = a.sm_scale;
   p.scale_log2 = a.sm_scale * kLog2e;
@@ -412,7 +423,7 @@ static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
 
-  auto kern = prefill_tc_kernel<D, NST, NP>;
+  auto kern = prefill_tc_kernel<D, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -435,8 +446,8 @@ int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
     set_error("GQA group of %d query heads exceeds the 128 rows of a tile", G);
     return SINKATTN_UNSUPPORTED;
   }
-  if (a.d == 64) return launch_tc<64, 3, 2>(a, stream);
-  return launch_tc<128, 2, 1>(a, stream);
+  if (a.d == 64) return launch_tc<64, 4>(a, stream);
+  return launch_tc<128, 2>(a, stream);
 }
 
 int read_status_prefill_tc(cudaStream_t s, int* status) {
