@@ -27,7 +27,11 @@
 //    the same TMEM region (so few registers are live). O_t is rescaled in
 //    TMEM when a row's maximum grows; the previous PV_t has completed by then,
 //    because S_t(j) is only issued after it. Row sums are kept both exact (for
-//    lse) and over the bf16-rounded weights the MMA applies (for out).
+//    lse) and over the bf16-rounded weights the MMA applies (for out). With
+//    d = 64 the second sum comes from the tensor core: the P.V MMA is 80
+//    columns wide, its extra 16 columns multiplying P by a shared-memory block
+//    of bf16 ones, so O_t's column 64 holds exactly the sum of the weights the
+//    MMA applied (TMEM has room for that only at d = 64).
 //
 // Every wait is bounded; on a timeout the CTA records SINKATTN_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
@@ -52,6 +56,8 @@ struct TcParams {
 
 template <int D, int NST>
 struct TcCfg {
+  static constexpr bool SUMCOL = (D == 64);       // row sums from the tensor core
+  static constexpr int NO = D + (SUMCOL ? 16 : 0);  // O_t columns
   static constexpr int NSUB = D / 64;
   static constexpr int KT = 128;                  // keys per KV tile
   static constexpr int SUB = 128 * 128;           // [128 rows][64 bf16], 128B-swizzled: 16 KB
@@ -60,14 +66,16 @@ struct TcCfg {
   static constexpr int STAGE = 2 * KV_TILE;       // K and V of one KV tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
-  static constexpr int OFF_BAR = OFF_KV + NST * STAGE;
+  static constexpr int OFF_ONES = OFF_KV + NST * STAGE;   // [128][64] bf16 ones (SUMCOL)
+  static constexpr int OFF_BAR = OFF_ONES + (SUMCOL ? SUB : 0);
   static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
   static constexpr int THREADS = 320;             // TMA, MMA, 2 x 4 softmax warps
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns: S_t (P_t in its first 64 columns) at 128 t, O_t at 256 + D t.
+  // TMEM columns: S_t (P_t in its first 64 columns) at 128 t, O_t at 256 + NO t.
   static constexpr uint32_t col_s(int t) { return 128u * t; }
-  static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(NO) * t; }
+  static_assert(256 + 2 * NO <= 512, "TMEM budget");
 };
 
 template <int D, int NST>
@@ -134,6 +142,12 @@ __global__ void __launch_bounds__(320, 1)
     tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc::tmem_relinquish();
   }
+  if (C::SUMCOL) {
+    uint4* ones = reinterpret_cast<uint4*>(smem + C::OFF_ONES);
+    const uint4 v1 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    for (int i = threadIdx.x; i < C::SUB / 16; i += blockDim.x) ones[i] = v1;
+    tc::fence_proxy_async_smem();   // read by the tensor core
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -180,7 +194,8 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
+      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, C::NO, true);
+      const uint32_t ones_base = smem_u32(smem + C::OFF_ONES);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       auto issue_s = [&](int t, int j) {
         const uint32_t k_base = smem_u32(smem + C::OFF_KV + (j % NST) * C::STAGE);
@@ -195,9 +210,11 @@ __global__ void __launch_bounds__(320, 1)
       };
       auto issue_pv = [&](int t, int j) {
         const uint32_t v_base = smem_u32(smem + C::OFF_KV + (j % NST) * C::STAGE + C::KV_TILE);
+        // the second 64-column block of B: V's own (d = 128) or the ones block
+        const uint32_t lbo = C::SUMCOL ? ones_base - v_base : static_cast<uint32_t>(C::SUB);
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk) {
-          const uint64_t bd = tc::smem_desc_sw128(v_base + kk * 2048, C::SUB, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(v_base + kk * 2048, lbo, 1024);
           tc::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, bd, idesc_o,
                      (j > 0 || kk > 0) ? 1u : 0u);
         }
@@ -249,7 +266,8 @@ __global__ void __launch_bounds__(320, 1)
     const float c2 = p.scale_log2;
 
     // l: exact running sum (for lse); lr: sum of the bf16-rounded weights the
-    // P.V MMA applies (for normalising out). Both include the sink's term.
+    // P.V MMA applies (for normalising out). Both include the sink's term; with
+    // the sum column, lr holds only the sink's term and the MMA adds the rest.
     float m_used = kNegInf, l = 0.f, lr = 0.f;
     if (p.sinks != nullptr && valid) {
       const float s = p.sinks[h];
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(320, 1)
           const float a1 = ex2(fmaf(v[e + 1], c2, -mb));
           rs4[(e >> 1) & 3] += a0 + a1;
           pk[e >> 1] = pack_bf16x2(a0, a1);
-          rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+          if (!C::SUMCOL) rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
         }
         tc::tmem_st16(s_addr + c * 16, pk);
       }
@@ -341,6 +359,14 @@ __global__ void __launch_bounds__(320, 1)
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
           tc::tmem_st32(o_addr + c * 32, o);
         }
+        if (C::SUMCOL) {
+          float o[16];
+          tc::tmem_ld16(o_addr + D, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] *= alpha;
+          tc::tmem_st16f(o_addr + D, o);
+        }
         tc::tmem_wait_st();
       }
       l = l * alpha + rs;
@@ -353,6 +379,12 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && n >= 1) {
       ok = wwait(&pv_done[t], (n - 1) & 1);
       tc::fence_after_sync();
+    }
+    if (C::SUMCOL && n >= 1 && ok) {
+      float o[16];
+      tc::tmem_ld16(o_addr + D, o);
+      tc::tmem_wait_ld();
+      lr += o[0];
     }
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
