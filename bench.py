@@ -459,8 +459,12 @@ def main():
                 tf = fl / (ms_a * 1e-3) / 1e12
                 also.append({"workload": _workload_desc(wa), "value": tf, "unit": "TFLOP/s",
                              "ms_per_step": ms_a, "frac_of_bf16": tf / peaks["bf16_tflops"],
+                             "peak_bf16_tflops": peaks["bf16_tflops"],
                              "hbm_gbs": nb / (ms_a * 1e-3) / 1e9,
-                             "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"]})
+                             "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "kernel": "prefill_tc_kernel (tcgen05)",
+                             "traffic": ncu_traffic("prefill_tc_kernel/" + name,
+                                                    ["prefill_tc.cu", "common.cuh", "tc.cuh"])})
             del inp_a
             torch.cuda.empty_cache()
 
