@@ -17,6 +17,8 @@
 //    the two tiles so the tensor core works on one while the other's softmax
 //    runs:  S_A(0), S_B(0), then per KV tile j:
 //           PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//    with every shared-memory descriptor prepared once, so a group of MMAs
+//    issues back to back;
 //    with S_t = Q_t K^T (M 128, N 128, K d; both operands in shared memory)
 //    and O_t += P_t V (M 128, N d, K 128; P_t read from TMEM, V from shared);
 //  * warps 2-9 / 10-17: softmax of tile A / B, two threads per row (= TMEM
@@ -75,8 +77,8 @@ struct TcCfg {
   static constexpr int THREADS = 576;             // TMA, MMA, 2 tiles x 2 halves x 4 softmax warps
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S_t (P_t in its first 64 columns) at 128 t, O_t at 256 + NO t.
-  static constexpr uint32_t col_s(int t) { return 128u * t; }
-  static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(NO) * t; }
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(NO) * t; }
   static_assert(256 + 2 * NO <= 512, "TMEM budget");
 };
 
@@ -200,29 +202,40 @@ __global__ void __launch_bounds__(576, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, C::NO, true);
-      const uint32_t ones_base = smem_u32(smem + C::OFF_ONES);
-      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      constexpr uint64_t STAGE16 = C::STAGE >> 4;   // one K/V stage, in descriptor address units
+      constexpr uint64_t SUB16 = C::SUB >> 4;
+      // Descriptors prepared once: a K step (16 elements = 32 bytes) within a
+      // 128-byte swizzle row adds 2 to the address field, the next 64-column
+      // block adds SUB / 16, a stage adds STAGE / 16, 16 keys of V add 128.
+      const uint64_t qd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t kd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+      // V's second 64-column block: its own (d = 128) or the ones block. The
+      // leading-dimension field then shrinks by one stage per stage.
+      const uint32_t v_base0 = smem_u32(smem + C::OFF_KV + C::KV_TILE);
+      const uint32_t lbo0 = C::SUMCOL ? smem_u32(smem + C::OFF_ONES) - v_base0
+                                      : static_cast<uint32_t>(C::SUB);
+      const uint64_t vd0 = tc::smem_desc_sw128(v_base0, lbo0, 1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t k_base = smem_u32(smem + C::OFF_KV + (j % NST) * C::STAGE);
-        const uint32_t qt = q_base + t * C::Q_TILE;
+        const uint64_t kd = kd0 + static_cast<uint64_t>(j % NST) * STAGE16;
+        const uint64_t qd = qd0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
+        const uint32_t d_tm = tmem + C::col_s(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = tc::smem_desc_sw128(qt + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(k_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
-          tc::mma_ss(tmem + C::col_s(t), a, bd, idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(kk >> 2) * SUB16 + static_cast<uint64_t>(kk & 3) * 2;
+          tc::mma_ss(d_tm, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc::commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v_base = smem_u32(smem + C::OFF_KV + (j % NST) * C::STAGE + C::KV_TILE);
-        // the second 64-column block of B: V's own (d = 128) or the ones block
-        const uint32_t lbo = C::SUMCOL ? ones_base - v_base : static_cast<uint32_t>(C::SUB);
+        const uint64_t st = static_cast<uint64_t>(j % NST);
+        const uint64_t vd = C::SUMCOL ? vd0 + st * STAGE16 - (st * STAGE16 << 16)
+                                      : vd0 + st * STAGE16;
+        const uint32_t d_tm = tmem + C::col_o(t);
+        const uint32_t a_tm = tmem + C::col_s(t);
 #pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          const uint64_t bd = tc::smem_desc_sw128(v_base + kk * 2048, lbo, 1024);
-          tc::mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, bd, idesc_o,
+        for (int kk = 0; kk < KT / 16; ++kk)
+          tc::mma_ts(d_tm, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u, idesc_o,
                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
         tc::commit(&pv_done[t]);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, status);
