@@ -59,10 +59,13 @@ struct MmaCfg {
   static constexpr int XCHG_BYTES = (TG - 1) * RT * 32 * XCHG_FLOATS_PER_LANE * 4;
   static constexpr int BAR_BYTES = 2 * NST * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + BAR_BYTES + XCHG_BYTES;
+  // Two resident CTAs per SM: one CTA's prologue (barrier set-up, first TMA
+  // round trip, Q fragments) and epilogue overlap the other's streaming.
+  static constexpr int MIN_CTAS = 2;
 };
 
 template <int D, int RT, int TG, int KT, int NST>
-__global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS)
+__global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D, RT, TG, KT, NST>::MIN_CTAS)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const MmaParams p) {
   using C = MmaCfg<D, RT, TG, KT, NST>;
