@@ -168,7 +168,7 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
     for _ in range(warmup):
         run()
     split_ms = None
-    if w.kind == "decode" and want_kernel_split:
+    if w.kind == "decode" and want_kernel_split and not run.fused:
         # split and merge launched separately with an event between them, so
         # the dominant kernel's own time is measured inside the timed region
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
@@ -202,6 +202,8 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
         e1.record(stream)
         _sync(dist_ctx)
         ms = e0.elapsed_time(e1) / steps
+        if w.kind == "decode":
+            split_ms = ms   # the fused kernel is the whole step
     ms = _max_over_ranks(ms, dist_ctx)
     if split_ms is not None:
         split_ms = _max_over_ranks(split_ms, dist_ctx)
@@ -221,6 +223,16 @@ def _max_over_ranks(x, ctx):
     return runner.max_over_ranks(x)
 
 
+def runner_call(run, inp):
+    """One pass of the runner's workload on the given (device) inputs."""
+    saved = run.inp
+    run.inp = inp
+    try:
+        return run()
+    finally:
+        run.inp = saved
+
+
 def e2e_decode(w, inp, run, steps):
     """Same metric through the C ABI with host buffers: H2D of the step's
     inputs from pinned memory, the decode, D2H of out + lse, all timed."""
@@ -233,13 +245,13 @@ def e2e_decode(w, inp, run, steps):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
+    run_dev = dict(inp)
+    run_dev.update(dev)
+
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        B.sinkattn_decode(dev["q"], dev["k"], dev["v"], dev["cu_k"], dev["sinks"], w.q_len,
-                          inp["max_k"], w.num_kv_heads, num_splits=run.num_splits, sm_scale=w.scale,
-                          causal=w.causal, window=w.window, workspace=run.workspace, out=run.out,
-                          lse=run.lse)
+        runner_call(run, run_dev)
         out_h.copy_(run.out, non_blocking=True)
         lse_h.copy_(run.lse, non_blocking=True)
 
@@ -442,8 +454,15 @@ def main():
     clocks = sampler.summary()
     nbytes, flops, split_bytes = work(w, inp)
     value = world * nbytes / (ms * 1e-3) / 1e9
+    if run.fused:
+        # one launch does split and merge: its algorithmic bytes are the step's
+        split_bytes = nbytes
+        kernel_name = "attn_mma_kernel, cluster-fused split-KV decode (%d chunks per cluster)" % run.num_splits
+    else:
+        kernel_name = "attn_mma_kernel (split-KV decode, then merge_kernel)"
     split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("attn_mma_kernel/" + HEADLINE, ["attn_mma.cu", "common.cuh"])
+    traffic = ncu_traffic(("attn_mma_kernel_fused/" if run.fused else "attn_mma_kernel/") + HEADLINE,
+                          ["attn_mma.cu", "common.cuh"])
 
     e2e = None
     if not args.no_e2e:
@@ -463,8 +482,8 @@ def main():
                 also.append({"workload": _workload_desc(wa), "value": nb / (ms_a * 1e-3) / 1e9,
                              "unit": "GB/s", "ms_per_step": ms_a,
                              "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "split_kernel_gbs": sb / (split_a * 1e-3) / 1e9,
-                             "num_splits": splits_of(wa, inp_a)})
+                             "num_splits": splits_of(wa, inp_a),
+                             "kernel": "attn_mma_kernel, cluster-fused split-KV decode"})
             else:
                 tf = fl / (ms_a * 1e-3) / 1e12
                 also.append({"workload": _workload_desc(wa), "value": tf, "unit": "TFLOP/s",
@@ -492,7 +511,7 @@ def main():
             "config": {"workload": _workload_desc(w), "num_splits": run.num_splits,
                        "l2": "inputs larger than L2 (%.0f MB of K/V per step vs 129 MB L2), no flush" % (split_bytes / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel (split-KV decode)",
+            "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "algorithmic_bytes_per_launch": split_bytes,
@@ -500,7 +519,7 @@ def main():
             "step_frac_of_hbm": value / world / peaks["hbm_gbs"],
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": run.launches_per_call * args.steps,
             "clocks": clocks,
             "also": also,
         }

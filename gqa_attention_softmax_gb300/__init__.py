@@ -2,7 +2,7 @@
 
 Public API (thin wrappers over the C ABI in ``include/sinkattn.h``):
 ``sinkattn_prefill``, ``sinkattn_decode_split``, ``sinkattn_merge``,
-``sinkattn_decode``, ``sinkattn_decode_noalloc``, ``sinkattn_decode_workspace_bytes``,
+``sinkattn_decode``, ``sinkattn_decode_fused``, ``sinkattn_decode_noalloc``, ``sinkattn_decode_workspace_bytes``,
 ``sinkattn_decode_default_splits``, ``sinkattn_status_string``,
 ``sinkattn_last_error``, ``sinkattn_debug_status``.
 
@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     sinkattn_debug_status,
     sinkattn_decode,
     sinkattn_decode_default_splits,
+    sinkattn_decode_fused,
     sinkattn_decode_noalloc,
     sinkattn_decode_split,
     sinkattn_decode_workspace_bytes,

@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
             L.sinkattn_merge.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P]
             L.sinkattn_decode.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, I32, F, I32, I32, I32,
                                           P, P, SZ, P, P, P]
+            L.sinkattn_decode_fused.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, I32, F, I32,
+                                                I32, I32, P, P, P, P]
             L.sinkattn_decode_noalloc.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, I32, F, I32,
                                                   I32, I32, P, P, P, P]
             L.sinkattn_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, I32,
@@ -59,7 +61,7 @@ def lib() -> ctypes.CDLL:
             L.sinkattn_last_error.restype = ctypes.c_char_p
             L.sinkattn_debug_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
             for name in ("sinkattn_prefill", "sinkattn_decode_split", "sinkattn_merge",
-                         "sinkattn_decode", "sinkattn_decode_noalloc", "sinkattn_decode_workspace_bytes",
+                         "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc", "sinkattn_decode_workspace_bytes",
                          "sinkattn_decode_default_splits", "sinkattn_debug_status"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -180,6 +182,26 @@ def sinkattn_decode(q, k, v, kv_indptr, sinks, q_len, max_kv_len, num_kv_heads, 
                                int(bool(causal)), int(window), int(num_splits), _ptr(sinks),
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _ptr(out), _ptr(lse), _stream(q, stream))
+    _check(rc)
+    return out, lse
+
+
+def sinkattn_decode_fused(q, k, v, kv_indptr, sinks, q_len, max_kv_len, num_kv_heads,
+                          num_splits=0, sm_scale=None, causal=True, window=0, out=None, lse=None,
+                          return_lse=True, stream=None):
+    """Split-KV decode / MTP with the merge done on chip by a thread-block
+    cluster (num_splits <= 16; no workspace). Returns (out, lse)."""
+    rows, Hq, d = q.shape
+    batch = kv_indptr.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
+    rc = lib().sinkattn_decode_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), batch,
+                                     int(q_len), int(max_kv_len), Hq, int(num_kv_heads), d,
+                                     _scale(sm_scale, d), int(bool(causal)), int(window),
+                                     int(num_splits), _ptr(sinks), _ptr(out), _ptr(lse),
+                                     _stream(q, stream))
     _check(rc)
     return out, lse
 

@@ -277,7 +277,7 @@ int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, int32_t num_qo_
   const int64_t cap = max_kv_len / (4 * kt);
   if (s > cap) s = cap;
   if (s < 1) s = 1;
-  if (s > 64) s = 64;
+  if (s > 16) s = 16;
   *num_splits = static_cast<int32_t>(s);
   return SINKATTN_OK;
 }
@@ -313,6 +313,45 @@ int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* 
   if (batch == 0) return SINKATTN_OK;
   return sinkattn_merge(part_acc, part_md, sinks, batch * q_len, num_qo_heads, head_dim,
                         num_splits, out, lse, stream);
+}
+
+int sinkattn_decode_fused(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
+                          int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
+                          int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
+                          int32_t window, int32_t num_splits, const float* sinks, void* out,
+                          float* lse, void* stream) {
+  g_last_error[0] = '\0';
+  int rc = check_common(q, k, v, num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window);
+  if (rc) return rc;
+  if (!kv_indptr) return fail(SINKATTN_INVALID_ARG, "kv_indptr must be non-null");
+  if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
+  if (batch < 0 || max_kv_len < 0) return fail(SINKATTN_INVALID_ARG, "sizes must be non-negative");
+  if (batch > 65535) return fail(SINKATTN_UNSUPPORTED, "batch %d exceeds 65535", batch);
+  if (q_len < 1) return fail(SINKATTN_INVALID_ARG, "q_len must be at least 1");
+  if (q_len > max_kv_len)
+    return fail(SINKATTN_INVALID_ARG, "q_len (%d) exceeds max_kv_len (%d)", q_len, max_kv_len);
+  if (num_qo_heads / num_kv_heads > 64)
+    return fail(SINKATTN_UNSUPPORTED, "GQA group of %d heads exceeds 64", num_qo_heads / num_kv_heads);
+  if (static_cast<int64_t>(num_kv_heads) * batch * max_kv_len >= (int64_t{1} << 31))
+    return fail(SINKATTN_UNSUPPORTED, "problem too large");
+  if (num_splits <= 0) {
+    rc = sinkattn_decode_default_splits(batch, q_len, num_qo_heads, num_kv_heads, head_dim,
+                                        max_kv_len, &num_splits);
+    if (rc) return rc;
+  }
+  if (num_splits > 16)
+    return fail(SINKATTN_UNSUPPORTED, "num_splits %d exceeds the 16 CTAs of a cluster", num_splits);
+  if (batch == 0) return SINKATTN_OK;
+  AttnArgs a{};
+  a.q = q; a.k = k; a.v = v;
+  a.cu_q = nullptr; a.cu_k = kv_indptr;
+  a.batch = batch; a.q_len = q_len; a.max_q = q_len; a.max_kv = max_kv_len;
+  a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
+  a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = num_splits;
+  a.sinks = sinks; a.out = out; a.lse = lse;
+  return launch_attn_mma_fused(a, static_cast<cudaStream_t>(stream));
 }
 
 int sinkattn_debug_status(void* stream, int* status) {

@@ -18,10 +18,17 @@
 //    ever reads past the last key the CTA needs; keys before the range that a
 //    tile covers are masked (and are real data or TMA zero-fill, never NaN).
 //
-// Output: the chunk's (m, d, acc) WITHOUT the sink; the merge kernel seeds
-// with the sink so it counts exactly once ("GPT-OSS on Day 0", section
-// "Kernels for GPT-OSS / Sink attention": online softmax with a running max,
-// the sink in one block only when the sequence is split).
+// Output, split mode: the chunk's (m, d, acc) WITHOUT the sink, to HBM; the
+// merge kernel seeds with the sink so it counts exactly once ("GPT-OSS on
+// Day 0", section "Kernels for GPT-OSS / Sink attention": online softmax with
+// a running max, the sink in one block only when the sequence is split).
+//
+// Output, fused mode: the S chunks of one (sequence, KV head, query block)
+// form a thread-block cluster. Each CTA leaves its partial in its own shared
+// memory; after a cluster barrier, CTA r folds rows r, r + S, ... of all S
+// partials read through distributed shared memory, seeded with the sink, and
+// writes out and lse; a second cluster barrier keeps every CTA's shared
+// memory alive until its peers have read it. No partials go to HBM.
 #include <cstdio>
 
 #include "common.cuh"
@@ -45,6 +52,9 @@ struct MmaParams {
   int causal, window;
   float* part_acc;
   float* part_md;
+  const float* sinks;     // fused mode
+  __nv_bfloat16* out;     // fused mode
+  float* lse;             // fused mode
 };
 
 template <int D, int RT, int TG, int KT, int NST>
@@ -59,12 +69,15 @@ struct MmaCfg {
   static constexpr int XCHG_BYTES = (TG - 1) * RT * 32 * XCHG_FLOATS_PER_LANE * 4;
   static constexpr int BAR_BYTES = 2 * NST * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + BAR_BYTES + XCHG_BYTES;
+  // fused mode: one CTA's partial, [16 RT rows][m, d, pad, pad, acc[D]], over the tile ring
+  static constexpr int XOUT_STRIDE = D + 4;
+  static_assert(16 * RT * XOUT_STRIDE * 4 <= NST * STAGE_BYTES, "partial fits in the tile ring");
   // Two resident CTAs per SM: one CTA's prologue (barrier set-up, first TMA
   // round trip, Q fragments) and epilogue overlap the other's streaming.
   static constexpr int MIN_CTAS = 2;
 };
 
-template <int D, int RT, int TG, int KT, int NST>
+template <int D, int RT, int TG, int KT, int NST, bool FUSED>
 __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D, RT, TG, KT, NST>::MIN_CTAS)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const MmaParams p) {
@@ -94,7 +107,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   const int k_start = p.cu_k[b];
   const int Lk = p.cu_k[b + 1] - k_start;
   const int q0 = qb * p.QB;
-  if (q0 >= Lq) return;   // uniform over the CTA, before any barrier
+  if (q0 >= Lq) return;   // uniform over the CTA (and the cluster), before any barrier
   const int nq = min(p.QB, Lq - q0);
   if (threadIdx.x == 0 && (Lk < Lq || Lk > p.max_kv || Lq < 0))
     atomicExch(&g_status_attn_mma, SINKATTN_BAD_LENGTHS);
@@ -122,6 +135,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   __syncthreads();
 
   // ------------------------------------------------------------------ producer
+  bool writer = false;   // consumer warps holding the CTA's combined state
   if (warp == NW) {
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&tmK);
@@ -149,9 +163,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
           mbar_drain(&full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
       }
     }
-    return;
-  }
-
+  } else {
   // ------------------------------------------------------------------ consumers
   const int rt = warp % RT;
   const int tg = warp / RT;
@@ -320,7 +332,9 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
       slot[D / 2 + 3] = l[1];
     }
     named_barrier_sync(1, NW * 32);
-    if (tg > 0) return;
+  }
+  writer = (tg == 0);
+  if (TG > 1 && writer) {
 #pragma unroll 1
     for (int t = 1; t < TG; ++t) {
       const float* slot = xchg + ((t - 1) * RT + rt) * 32 * C::XCHG_FLOATS_PER_LANE +
@@ -347,11 +361,11 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   }
 
   // ------------------------------------------------------------------ epilogue
+  if (!FUSED && writer) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if (!valid[i]) continue;
-    const size_t rowid = static_cast<size_t>(tok[i]) * p.Hq + head[i];
-    {
+    for (int i = 0; i < 2; ++i) {
+      if (!valid[i]) continue;
+      const size_t rowid = static_cast<size_t>(tok[i]) * p.Hq + head[i];
       float* arow = p.part_acc + (rowid * S + split) * D;
 #pragma unroll
       for (int jd = 0; jd < D / 8; ++jd) {
@@ -366,12 +380,92 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
       }
     }
   }
+  if (FUSED && writer) {
+    // this CTA's partial (raw-logit m, d, acc) into its own shared memory; the
+    // tile ring is free: every tile has been consumed
+    float* xout = reinterpret_cast<float*>(tiles);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = rt * 16 + (lane >> 2) + 8 * i;
+      float* xr = xout + r * C::XOUT_STRIDE;
+#pragma unroll
+      for (int jd = 0; jd < D / 8; ++jd) {
+        const int col = jd * 8 + (lane & 3) * 2;
+        *reinterpret_cast<float2*>(xr + 4 + col) = make_float2(o[jd][2 * i], o[jd][2 * i + 1]);
+      }
+      if ((lane & 3) == 0) {
+        xr[0] = m[i];
+        xr[1] = l[i];
+      }
+    }
+  }
+  }   // consumers
+
+  if (FUSED) {
+    cluster_sync_all();
+    // Fold rows rank, rank + S, ... over the S partials of the cluster, seeded
+    // with the sink (the sink counts once). One consumer warp per row; lane s
+    // reads peer s's (m, d); each lane owns D/32 output columns.
+    constexpr int VEC = D / 32;
+    const float* xout = reinterpret_cast<const float*>(tiles);
+    const uint32_t rank = static_cast<uint32_t>(split);
+    if (warp < NW) {
+      const float c2 = p.scale_log2;
+      for (int r = static_cast<int>(rank) + S * warp; r < 16 * RT; r += S * NW) {
+        const int tl = r / p.G;
+        if (tl >= nq) continue;
+        const int tk = q_start + q0 + tl;
+        const int hh = kvh * p.G + (r - tl * p.G);
+        const float* xr = xout + r * C::XOUT_STRIDE;
+        float ms = NEG_INF, ls = 0.f;
+        if (lane < S) {
+          ms = ld_dsmem(xr + 0, static_cast<uint32_t>(lane));
+          ls = ld_dsmem(xr + 1, static_cast<uint32_t>(lane));
+        }
+        float M = ms;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float sk = p.sinks ? p.sinks[hh] : NEG_INF;
+        const float sink_raw = (sk == NEG_INF) ? NEG_INF : sk / p.sm_scale;
+        M = fmaxf(M, sink_raw);
+        const float ws = (ms == NEG_INF) ? 0.f : ex2((ms - M) * c2);
+        float L = ws * ls;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (sink_raw != NEG_INF) L += ex2((sink_raw - M) * c2);
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) {
+          const float w = __shfl_sync(0xffffffffu, ws, s2);
+          if (w == 0.f) continue;
+          float v[VEC];
+          ld_dsmem_vec<VEC>(xr + 4 + lane * VEC, static_cast<uint32_t>(s2), v);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        __nv_bfloat16* orow = p.out + (static_cast<size_t>(tk) * p.Hq + hh) * D + lane * VEC;
+        if constexpr (VEC == 4) {
+          uint2 pk;
+          pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+          pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+          *reinterpret_cast<uint2*>(orow) = pk;
+        } else {
+          *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
+        if (p.lse != nullptr && lane == 0)
+          p.lse[static_cast<size_t>(tk) * p.Hq + hh] = L > 0.f ? (M * c2 + lg2(L)) * kLn2 : NEG_INF;
+      }
+    }
+    cluster_sync_all();   // peers may still be reading this CTA's partial
+  }
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int D, int RT, int TG, int KT, int NST>
+template <int D, int RT, int TG, int KT, int NST, bool FUSED>
 static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   using C = MmaCfg<D, RT, TG, KT, NST>;
   CUtensorMap tmK, tmV;
@@ -400,8 +494,11 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   p.window = a.window;
   p.part_acc = a.part_acc;
   p.part_md = a.part_md;
+  p.sinks = a.sinks;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
 
-  auto kern = attn_mma_kernel<D, RT, TG, KT, NST>;
+  auto kern = attn_mma_kernel<D, RT, TG, KT, NST, FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) {
@@ -410,8 +507,32 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   }
   const dim3 grid(static_cast<unsigned>(p.nqb * p.num_splits), static_cast<unsigned>(a.Hkv),
                   static_cast<unsigned>(a.batch));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmK, tmV, p);
-  e = cudaGetLastError();
+  if (FUSED) {
+    // the S chunks of one (sequence, KV head, query block) form a cluster
+    if (p.num_splits > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) {
+        set_error("cluster size %d not allowed: %s", p.num_splits, cudaGetErrorString(e));
+        return SINKATTN_UNSUPPORTED;
+      }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.num_splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tmK, tmV, p);
+  } else {
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmK, tmV, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) {
     set_error("attention kernel launch: %s", cudaGetErrorString(e));
     return SINKATTN_CUDA_ERROR;
@@ -419,7 +540,8 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   return SINKATTN_OK;
 }
 
-int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
+template <bool FUSED>
+static int launch_attn_mma_t(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   const int rows = G * a.q_len;
   const int rt_needed = (rows + 15) / 16;
@@ -428,15 +550,23 @@ int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
     return SINKATTN_UNSUPPORTED;
   }
   if (a.d == 64) {
-    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4>(a, stream);
-    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4>(a, stream);
-    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4>(a, stream);
-    return launch_cfg<64, 4, 2, 64, 4>(a, stream);
+    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4, FUSED>(a, stream);
+    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4, FUSED>(a, stream);
+    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4, FUSED>(a, stream);
+    return launch_cfg<64, 4, 2, 64, 4, FUSED>(a, stream);
   }
-  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4>(a, stream);
-  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4>(a, stream);
-  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4>(a, stream);
-  return launch_cfg<128, 4, 2, 32, 4>(a, stream);
+  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4, FUSED>(a, stream);
+  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4, FUSED>(a, stream);
+  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4, FUSED>(a, stream);
+  return launch_cfg<128, 4, 2, 32, 4, FUSED>(a, stream);
+}
+
+int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
+  return launch_attn_mma_t<false>(a, stream);
+}
+
+int launch_attn_mma_fused(const AttnArgs& a, cudaStream_t stream) {
+  return launch_attn_mma_t<true>(a, stream);
 }
 
 int read_status_attn_mma(cudaStream_t s, int* status) {

@@ -43,6 +43,11 @@ int make_q_tmap(CUtensorMap* map, const void* q, uint64_t total_q, int Hq, int d
 // path. Returns a SINKATTN_* status.
 int launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 
+// Split-KV decode with the merge done on chip: the num_splits (<= 16) chunks
+// of one (sequence, KV head) form a thread-block cluster that folds its
+// partials through distributed shared memory. Writes out / lse directly.
+int launch_attn_mma_fused(const AttnArgs& a, cudaStream_t stream);
+
 // Single-pass prefill on the tcgen05/TMEM path. Returns a SINKATTN_* status.
 int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
 

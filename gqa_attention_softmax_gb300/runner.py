@@ -25,20 +25,33 @@ class Runner:
     """Holds the output / workspace buffers of one workload so repeated calls
     allocate nothing."""
 
-    def __init__(self, w: Workload, inp: dict):
+    def __init__(self, w: Workload, inp: dict, fused: bool = False):
         self.w, self.inp = w, inp
         dev = inp["q"].device
         self.out = torch.empty_like(inp["q"])
         self.lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=dev)
         self.num_splits = splits_for(w, inp)
+        # decode: split + merge through a workspace. The cluster-fused form
+        # (sinkattn_decode_fused) is available but measured slower on the
+        # gpt-oss- and Qwen-shaped decodes, so it is opt-in.
+        self.fused = w.kind == "decode" and fused and self.num_splits <= 16
         self.workspace = None
-        if w.kind == "decode":
+        if w.kind == "decode" and not self.fused:
             n = B.sinkattn_decode_workspace_bytes(inp["batch"], w.q_len, w.num_qo_heads, w.head_dim,
                                                   self.num_splits)
             self.workspace = torch.empty((max(n, 256),), dtype=torch.uint8, device=dev)
 
+    @property
+    def launches_per_call(self) -> int:
+        return 2 if (self.w.kind == "decode" and not self.fused) else 1
+
     def __call__(self, stream=None):
         w, i = self.w, self.inp
+        if w.kind == "decode" and self.fused:
+            return B.sinkattn_decode_fused(i["q"], i["k"], i["v"], i["cu_k"], i["sinks"], w.q_len,
+                                           i["max_k"], w.num_kv_heads, num_splits=self.num_splits,
+                                           sm_scale=w.scale, causal=w.causal, window=w.window,
+                                           out=self.out, lse=self.lse, stream=stream)
         if w.kind == "decode":
             return B.sinkattn_decode(i["q"], i["k"], i["v"], i["cu_k"], i["sinks"], w.q_len,
                                      i["max_k"], w.num_kv_heads, num_splits=self.num_splits,

@@ -142,6 +142,27 @@ SINKATTN_API int sinkattn_decode(const void* q, const void* k, const void* v, co
                     size_t workspace_bytes, void* out, float* lse, void* stream);
 
 /*
+ * Split-KV decode / MTP with the merge done on chip (no workspace): the
+ * num_splits chunks of one (sequence, KV head) run as one thread-block
+ * cluster; each chunk's partial (m, d, acc) stays in its CTA's shared memory
+ * and the cluster folds them through distributed shared memory, seeding the
+ * running state with the sink so it counts exactly once ("GPT-OSS on Day 0",
+ * section "Kernels for GPT-OSS / Sink attention": parallel over heads and KV
+ * length, the sink in one block only). Same chunking and results as
+ * sinkattn_decode_split followed by sinkattn_merge.
+ *   Arguments as sinkattn_decode without the workspace; num_splits <= 0
+ *   selects sinkattn_decode_default_splits(); 1 <= num_splits <= 16 (a
+ *   cluster of more than 16 CTAs is not launched: SINKATTN_UNSUPPORTED).
+ *   out [batch*q_len, Hq, d] bf16; lse [batch*q_len, Hq] fp32 or NULL.
+ */
+SINKATTN_API int sinkattn_decode_fused(const void* q, const void* k, const void* v,
+                                       const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                                       int32_t max_kv_len, int32_t num_qo_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, float sm_scale,
+                                       int32_t causal, int32_t window, int32_t num_splits,
+                                       const float* sinks, void* out, float* lse, void* stream);
+
+/*
  * sinkattn_decode for callers that cannot allocate device memory (for example
  * code inside another runtime whose memory manager owns all device memory and
  * gives plugins no allocator, or loops where a cudaMalloc, which may
@@ -173,10 +194,10 @@ SINKATTN_API int sinkattn_decode_workspace_bytes(int32_t batch, int32_t q_len, i
                                     int32_t head_dim, int32_t num_splits, size_t* bytes);
 
 /*
- * The split count sinkattn_decode uses when given num_splits <= 0: enough
- * (sequence, KV head, chunk) work items to fill every SM several times over,
- * without chunks shorter than a few KV tiles. Host only; queries the current
- * device's SM count once.
+ * The split count sinkattn_decode and sinkattn_decode_fused use when given
+ * num_splits <= 0: enough (sequence, KV head, chunk) work items to fill every
+ * SM several times over, without chunks shorter than a few KV tiles; at most
+ * 16. Host only; queries the current device's SM count once.
  */
 SINKATTN_API int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, int32_t num_qo_heads,
                                    int32_t num_kv_heads, int32_t head_dim, int32_t max_kv_len,

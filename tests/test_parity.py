@@ -180,3 +180,44 @@ def test_outputs_are_deterministic():
     r2 = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], 3, 900, 4, num_splits=7)
     torch.cuda.synchronize()
     assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: "b%d_q%d_h%d-%d_d%d_k%d-%d_s%d_w%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5][0], c[5][1], c[6], c[7]))
+def test_fused_decode_matches_oracle(case):
+    """The cluster-fused decode (merge on chip through distributed shared
+    memory) against the unsplit oracle; more than 16 chunks is rejected."""
+    B, q_len, Hq, Hkv, d, kvr, S, window = case
+    inp = _decode_inputs(B, q_len, Hq, Hkv, d, kvr, seed=61 + S)
+    scale = 1.0 / math.sqrt(d)
+    g = to_dev(inp)
+    max_kv = max(inp["kv_lens"])
+    if S > 16:
+        with pytest.raises(sa.SinkAttnError) as e:
+            sa.sinkattn_decode_fused(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], q_len, max_kv,
+                                     Hkv, num_splits=S, sm_scale=scale, window=window)
+        assert e.value.status == 2
+        S = 16
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, True, window)
+    out, lse = sa.sinkattn_decode_fused(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], q_len, max_kv,
+                                        Hkv, num_splits=S, sm_scale=scale, window=window)
+    torch.cuda.synchronize()
+    compare(out, lse, want_out, want_lse, "fused decode S=%d" % S)
+    # and it equals split + merge up to rounding
+    out2, lse2 = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], q_len, max_kv,
+                                    Hkv, num_splits=S, sm_scale=scale, window=window)
+    torch.cuda.synchronize()
+    assert (out.float() - out2.float()).abs().max().item() <= 1e-2
+    assert (lse - lse2).abs().max().item() <= 1e-4
+
+
+def test_fused_decode_no_sink_and_default_splits():
+    inp = _decode_inputs(5, 2, 32, 4, 64, (2, 3000), seed=71)
+    g = to_dev(inp)
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], None, inp["cu_q"], inp["cu_k"],
+                                       32, 4, 64, 0.125, True, 0)
+    out, lse = sa.sinkattn_decode_fused(g["q"], g["k"], g["v"], g["cu_k"], None, 2,
+                                        max(inp["kv_lens"]), 4, num_splits=0, sm_scale=0.125)
+    torch.cuda.synchronize()
+    compare(out, lse, want_out, want_lse, "fused decode, no sink")
