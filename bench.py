@@ -391,6 +391,11 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def decode_kernel_name(w):
+    """The split kernel the library's default selection runs for this shape."""
+    return "decode_tc_kernel (tcgen05)" if w.head_dim == 128 else "attn_mma_kernel (mma.sync)"
+
+
 def _workload_desc(w):
     if w.kind == "decode":
         return ("%s: batch %d, %d query / %d KV heads, head_dim %d, q_len %d, kv_len ~ U[%d, %d], "
@@ -459,7 +464,7 @@ def main():
         split_bytes = nbytes
         kernel_name = "attn_mma_kernel, cluster-fused split-KV decode (%d chunks per cluster)" % run.num_splits
     else:
-        kernel_name = "attn_mma_kernel (split-KV decode, then merge_kernel)"
+        kernel_name = decode_kernel_name(w) + " (split-KV partials, then merge_kernel)"
     split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
     traffic = ncu_traffic(("attn_mma_kernel_fused/" if run.fused else "attn_mma_kernel/") + HEADLINE,
                           ["attn_mma.cu", "common.cuh"])
@@ -483,7 +488,7 @@ def main():
                              "unit": "GB/s", "ms_per_step": ms_a,
                              "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
                              "num_splits": splits_of(wa, inp_a),
-                             "kernel": "attn_mma_kernel, cluster-fused split-KV decode"})
+                             "kernel": decode_kernel_name(wa) + " + merge_kernel"})
             else:
                 tf = fl / (ms_a * 1e-3) / 1e12
                 also.append({"workload": _workload_desc(wa), "value": tf, "unit": "TFLOP/s",

@@ -60,9 +60,11 @@ def lib() -> ctypes.CDLL:
             L.sinkattn_last_error.argtypes = []
             L.sinkattn_last_error.restype = ctypes.c_char_p
             L.sinkattn_debug_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+            L.sinkattn_set_decode_kernel.argtypes = [ctypes.c_int]
             for name in ("sinkattn_prefill", "sinkattn_decode_split", "sinkattn_merge",
-                         "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc", "sinkattn_decode_workspace_bytes",
-                         "sinkattn_decode_default_splits", "sinkattn_debug_status"):
+                         "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc",
+                         "sinkattn_decode_workspace_bytes", "sinkattn_decode_default_splits",
+                         "sinkattn_debug_status", "sinkattn_set_decode_kernel"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -225,6 +227,16 @@ def sinkattn_decode_noalloc(q, k, v, kv_indptr, sinks, q_len, max_kv_len, num_kv
                                        _stream(q, stream))
     _check(rc)
     return out, lse
+
+
+DECODE_KERNELS = {"auto": 0, "warp": 1, "tcgen05": 2}
+
+
+def sinkattn_set_decode_kernel(kind) -> None:
+    """Selects the split-KV partial kernel process-wide: "auto", "warp" or
+    "tcgen05" (or the integer codes of include/sinkattn.h)."""
+    code = DECODE_KERNELS[kind] if isinstance(kind, str) else int(kind)
+    _check(lib().sinkattn_set_decode_kernel(code))
 
 
 def sinkattn_status_string(status: int) -> str:

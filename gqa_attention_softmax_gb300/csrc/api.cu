@@ -4,6 +4,7 @@
 // synchronises (except the diagnostic sinkattn_debug_status).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -16,6 +17,7 @@
 namespace sinkattn {
 
 static thread_local char g_last_error[512] = "";
+static std::atomic<int> g_decode_kernel{SINKATTN_DECODE_AUTO};
 
 void set_error(const char* fmt, ...) {
   va_list ap;
@@ -191,17 +193,19 @@ int sinkattn_prefill(const void* q, const void* k, const void* v, const float* s
   return launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
 }
 
-int sinkattn_decode_split(const void* q, const void* k, const void* v,
-                          const int32_t* kv_indptr, int32_t batch, int32_t q_len,
-                          int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
-                          int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
-                          int32_t num_splits, float* part_acc, float* part_md, void* stream) {
-  g_last_error[0] = '\0';
+}  // extern "C"
+
+namespace {
+
+// Validation shared by the split-KV decode entry points; fills `a` (without
+// the output pointers). Returns SINKATTN_OK or the failing status.
+int decode_args(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
+                int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
+                int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
+                int32_t window, int32_t num_splits, AttnArgs* a) {
   int rc = check_common(q, k, v, num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window);
   if (rc) return rc;
   if (!kv_indptr) return fail(SINKATTN_INVALID_ARG, "kv_indptr must be non-null");
-  if (!part_acc || !part_md || !aligned16(part_acc) || !aligned16(part_md))
-    return fail(SINKATTN_INVALID_ARG, "partial buffers must be non-null and 16-byte aligned");
   if (batch < 0 || max_kv_len < 0) return fail(SINKATTN_INVALID_ARG, "sizes must be non-negative");
   if (batch > 65535) return fail(SINKATTN_UNSUPPORTED, "batch %d exceeds 65535", batch);
   if (q_len < 1) return fail(SINKATTN_INVALID_ARG, "q_len must be at least 1");
@@ -215,16 +219,55 @@ int sinkattn_decode_split(const void* q, const void* k, const void* v,
       static_cast<int64_t>(batch) * q_len * num_qo_heads * num_splits * head_dim >=
           (int64_t{1} << 40))
     return fail(SINKATTN_UNSUPPORTED, "problem too large");
-  if (batch == 0) return SINKATTN_OK;
+  *a = AttnArgs{};
+  a->q = q; a->k = k; a->v = v;
+  a->cu_q = nullptr; a->cu_k = kv_indptr;
+  a->batch = batch; a->q_len = q_len; a->max_q = q_len; a->max_kv = max_kv_len;
+  a->Hq = num_qo_heads; a->Hkv = num_kv_heads; a->d = head_dim;
+  a->sm_scale = sm_scale; a->causal = causal; a->window = window; a->num_splits = num_splits;
+  return SINKATTN_OK;
+}
 
-  AttnArgs a{};
-  a.q = q; a.k = k; a.v = v;
-  a.cu_q = nullptr; a.cu_k = kv_indptr;
-  a.batch = batch; a.q_len = q_len; a.max_q = q_len; a.max_kv = max_kv_len;
-  a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
-  a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = num_splits;
+// Partials with the selected kernel (a.part_acc / a.part_md set).
+int launch_partials(const AttnArgs& a, cudaStream_t stream) {
+  const int kind = g_decode_kernel.load(std::memory_order_relaxed);
+  const bool tc_ok = decode_tc_supported(a);
+  if (kind == SINKATTN_DECODE_TCGEN05 && !tc_ok)
+    return fail(SINKATTN_UNSUPPORTED,
+                "the tcgen05 decode kernel needs head_dim 128");
+  if (kind == SINKATTN_DECODE_TCGEN05 || (kind == SINKATTN_DECODE_AUTO && tc_ok))
+    return launch_decode_tc(a, stream);
+  return launch_attn_mma(a, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sinkattn_decode_split(const void* q, const void* k, const void* v,
+                          const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                          int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                          int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
+                          int32_t num_splits, float* part_acc, float* part_md, void* stream) {
+  g_last_error[0] = '\0';
+  AttnArgs a;
+  int rc = decode_args(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads, num_kv_heads,
+                       head_dim, sm_scale, causal, window, num_splits, &a);
+  if (rc) return rc;
+  if (!part_acc || !part_md || !aligned16(part_acc) || !aligned16(part_md))
+    return fail(SINKATTN_INVALID_ARG, "partial buffers must be non-null and 16-byte aligned");
+  if (batch == 0) return SINKATTN_OK;
   a.part_acc = part_acc; a.part_md = part_md;
-  return launch_attn_mma(a, static_cast<cudaStream_t>(stream));
+  return launch_partials(a, static_cast<cudaStream_t>(stream));
+}
+
+int sinkattn_set_decode_kernel(int kind) {
+  g_last_error[0] = '\0';
+  if (kind != SINKATTN_DECODE_AUTO && kind != SINKATTN_DECODE_WARP &&
+      kind != SINKATTN_DECODE_TCGEN05)
+    return fail(SINKATTN_INVALID_ARG, "unknown decode kernel %d", kind);
+  g_decode_kernel.store(kind, std::memory_order_relaxed);
+  return SINKATTN_OK;
 }
 
 int sinkattn_merge(const float* part_acc, const float* part_md, const float* sinks, int32_t rows,
@@ -358,11 +401,12 @@ int sinkattn_debug_status(void* stream, int* status) {
   g_last_error[0] = '\0';
   if (!status) return fail(SINKATTN_INVALID_ARG, "status must be non-null");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int a = 0, m = 0, t = 0;
-  if (read_status_attn_mma(s, &a) || read_status_merge(s, &m) || read_status_prefill_tc(s, &t))
+  int a = 0, m = 0, t = 0, dt = 0;
+  if (read_status_attn_mma(s, &a) || read_status_merge(s, &m) || read_status_prefill_tc(s, &t) ||
+      read_status_decode_tc(s, &dt))
     return fail(SINKATTN_CUDA_ERROR, "reading the device status failed: %s",
                 cudaGetErrorString(cudaGetLastError()));
-  *status = a ? a : (t ? t : m);
+  *status = a ? a : (dt ? dt : (t ? t : m));
   return SINKATTN_OK;
 }
 

@@ -48,6 +48,13 @@ int launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 // partials through distributed shared memory. Writes out / lse directly.
 int launch_attn_mma_fused(const AttnArgs& a, cudaStream_t stream);
 
+
+// Split-KV decode on the tcgen05/TMEM path (head_dim 128; 16, 32, 48 or 64
+// query rows per KV head and query block). Same partial layout as
+// launch_attn_mma.
+bool decode_tc_supported(const AttnArgs& a);
+int launch_decode_tc(const AttnArgs& a, cudaStream_t stream);
+
 // Single-pass prefill on the tcgen05/TMEM path. Returns a SINKATTN_* status.
 int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
 
@@ -59,6 +66,7 @@ int launch_merge(const float* part_acc, const float* part_md, const float* sinks
 int read_status_attn_mma(cudaStream_t s, int* status);
 int read_status_merge(cudaStream_t s, int* status);
 int read_status_prefill_tc(cudaStream_t s, int* status);
+int read_status_decode_tc(cudaStream_t s, int* status);
 
 // Thread-local error text used by the C ABI.
 void set_error(const char* fmt, ...);

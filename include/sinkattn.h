@@ -132,8 +132,9 @@ SINKATTN_API int sinkattn_merge(const float* part_acc, const float* part_md, con
 /*
  * Split-KV decode / MTP in one call: sinkattn_decode_split then sinkattn_merge
  * on the same stream, with the partials in the caller's workspace (at least
- * sinkattn_decode_workspace_bytes() bytes, 256-byte aligned).
- * num_splits <= 0 selects sinkattn_decode_default_splits().
+ * sinkattn_decode_workspace_bytes() bytes, 256-byte aligned, device memory;
+ * contents on entry do not matter). num_splits <= 0 selects
+ * sinkattn_decode_default_splits().
  */
 SINKATTN_API int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
                     int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
@@ -202,6 +203,24 @@ SINKATTN_API int sinkattn_decode_workspace_bytes(int32_t batch, int32_t q_len, i
 SINKATTN_API int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, int32_t num_qo_heads,
                                    int32_t num_kv_heads, int32_t head_dim, int32_t max_kv_len,
                                    int32_t* num_splits);
+
+/*
+ * Which kernel computes the split-KV partials (sinkattn_decode_split, and so
+ * sinkattn_decode and sinkattn_decode_noalloc). Process-wide, host only.
+ *   SINKATTN_DECODE_AUTO (0, default): the tcgen05 kernel at head_dim 128,
+ *     the warp-level kernel at head_dim 64;
+ *   SINKATTN_DECODE_WARP (1): the warp-level (mma.sync) kernel;
+ *   SINKATTN_DECODE_TCGEN05 (2): the tcgen05/TMEM kernel (head_dim 128;
+ *     the query tokens x heads of a GQA group fill up to 128 MMA rows, e.g.
+ *     3 MTP tokens x 16 heads = 48); head_dim 64 then returns
+ *     SINKATTN_UNSUPPORTED.
+ * Both kernels produce the same partial layout and meaning. Returns
+ * SINKATTN_INVALID_ARG for any other value.
+ */
+#define SINKATTN_DECODE_AUTO 0
+#define SINKATTN_DECODE_WARP 1
+#define SINKATTN_DECODE_TCGEN05 2
+SINKATTN_API int sinkattn_set_decode_kernel(int kind);
 
 /* Human-readable name of a status code (static string). */
 SINKATTN_API const char* sinkattn_status_string(int status);

@@ -114,12 +114,24 @@ DECODE_CASES = [
     (1, 1, 64, 1, 64, (50, 70), 1, 0),       # GQA 64: four warp tiles
     (2, 5, 16, 1, 128, (5, 90), 2, 0),       # 80 rows: two query blocks
     (5, 2, 12, 3, 64, (2, 333), 5, 0),       # GQA 4 with odd head count
+    (2, 1, 32, 2, 128, (1, 700), 3, 0),      # 16 rows per block (tcgen05 N = 16)
+    (2, 2, 64, 4, 128, (2, 1500), 2, 64),    # 32 rows, window 64
+    (1, 3, 64, 4, 128, (1900, 2100), 1, 0),  # one chunk of 16 tiles: 4 TMEM groups
 ]
 
 
 @pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: "b%d_q%d_h%d-%d_d%d_k%d-%d_s%d_w%d" % (
     c[0], c[1], c[2], c[3], c[4], c[5][0], c[5][1], c[6], c[7]))
-def test_decode_split_merge_matches_oracle(case):
+@pytest.mark.parametrize("kernel", ["auto", "warp"])
+def test_decode_split_merge_matches_oracle(case, kernel):
+    sa.sinkattn_set_decode_kernel(kernel)
+    try:
+        _decode_split_merge(case)
+    finally:
+        sa.sinkattn_set_decode_kernel("auto")
+
+
+def _decode_split_merge(case):
     B, q_len, Hq, Hkv, d, kvr, S, window = case
     inp = _decode_inputs(B, q_len, Hq, Hkv, d, kvr, seed=31 + S)
     scale = 1.0 / math.sqrt(d)
@@ -159,6 +171,67 @@ def test_decode_split_merge_matches_oracle(case):
                                   Hkv, num_splits=S, sm_scale=scale, window=window)
     torch.cuda.synchronize()
     compare(out, lse, want_out, want_lse, "decode")
+
+
+TC_DECODE_CASES = [
+    # B, q_len, Hq, Hkv, G*QB rows, kv_range, S, window, q_scale
+    (3, 1, 64, 4, (1, 900), 2, 0, 3.0),        # 16 rows
+    (2, 4, 64, 8, (4, 1300), 1, 0, 3.0),       # GQA 8 x 4 tokens: 32 rows, 3 groups of tiles
+    (4, 3, 64, 4, (3, 2600), 2, 0, 4.0),       # 48 rows, peaky logits
+    (2, 4, 32, 2, (4, 700), 3, 100, 1.0),      # 64 rows, window 100
+    (3, 7, 32, 2, (7, 400), 2, 0, 1.0),        # 64 rows: query blocks of 4 and 3 tokens
+]
+
+
+@pytest.mark.parametrize("case", TC_DECODE_CASES, ids=lambda c: "b%d_q%d_h%d-%d_k%d-%d_s%d_w%d_x%g" % (
+    c[0], c[1], c[2], c[3], c[4][0], c[4][1], c[5], c[6], c[7]))
+def test_tcgen05_decode_partials(case):
+    """The tcgen05 split kernel forced on, partials against the oracle's;
+    peaky logits and chunks longer than one TMEM group of tiles."""
+    B, q_len, Hq, Hkv, kvr, S, window, qs = case
+    d = 128
+    inp = _decode_inputs(B, q_len, Hq, Hkv, d, kvr, seed=71 + S, q_scale=qs)
+    scale = 1.0 / math.sqrt(d)
+    g = to_dev(inp)
+    max_kv = max(inp["kv_lens"])
+    sa.sinkattn_set_decode_kernel("tcgen05")
+    try:
+        acc, md = sa.sinkattn_decode_split(g["q"], g["k"], g["v"], g["cu_k"], q_len, max_kv, Hkv,
+                                           S, scale, True, window)
+        out, lse = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], q_len, max_kv,
+                                      Hkv, num_splits=S, sm_scale=scale, window=window)
+        torch.cuda.synchronize()
+    finally:
+        sa.sinkattn_set_decode_kernel("auto")
+    acc_o, m_o, d_o = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"],
+                                            Hq, Hkv, d, scale, True, window, S)
+    acc_g, md_g = acc.cpu().numpy(), md.cpu().numpy()
+    m_g, d_g = md_g[..., 0], md_g[..., 1]
+    empty = np.isneginf(m_o)
+    assert (np.isneginf(m_g) == empty).all()
+    assert (d_g[empty] == 0).all() and (acc_g[empty] == 0).all()
+    ne = ~empty
+    assert np.abs(m_g[ne] - m_o[ne]).max() <= TOL_LSE
+    assert np.abs(np.log(d_g[ne]) - np.log(d_o[ne])).max() <= TOL_LSE
+    og = acc_g[ne] / d_g[ne][:, None]
+    oo = acc_o[ne] / d_o[ne][:, None]
+    assert np.abs(og - oo).max() <= TOL_MAX and np.abs(og - oo).mean() <= TOL_MEAN
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, True, window)
+    compare(out, lse, want_out, want_lse, "tcgen05 decode")
+
+
+def test_tcgen05_decode_rejects_unsupported_shape():
+    inp = _decode_inputs(2, 1, 64, 8, 64, (10, 100), seed=3)
+    g = to_dev(inp)
+    sa.sinkattn_set_decode_kernel("tcgen05")
+    try:
+        with pytest.raises(sa.SinkAttnError) as e:
+            sa.sinkattn_decode_split(g["q"], g["k"], g["v"], g["cu_k"], 1, 100, 8, 2, 0.125,
+                                     True, 0)
+        assert e.value.status == 2
+    finally:
+        sa.sinkattn_set_decode_kernel("auto")
 
 
 def test_decode_default_splits_and_no_sink():
