@@ -34,6 +34,8 @@
 // streaming while the other is in its prologue or epilogue. The partial rows
 // are staged in the (then idle) ring and written with coalesced stores.
 // Every wait is bounded.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -45,42 +47,96 @@ __device__ int g_status_decode_tc;
 struct DtcParams {
   const int32_t* cu_k;
   int q_len, Hq, Hkv, G, QB, nqb, num_splits, max_kv;
+  int n_items;   // batch * Hkv * nqb * num_splits
   float sm_scale, scale_log2;
   int causal, window;
   float* part_acc;
   float* part_md;
 };
 
+// One work item: (sequence b, KV head, query block, KV chunk) and its keys.
+struct DtcItem {
+  int b, kvh, split, q_start, q0, nq, k_start, Lk, pos0, k_lo, k_hi, n;
+};
+
+template <int KT>
+__device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, int it) {
+  DtcItem t;
+  const int S = p.num_splits;
+  t.split = it % S;
+  int r = it / S;
+  const int qb = p.nqb - 1 - r % p.nqb;   // longer query blocks first
+  r /= p.nqb;
+  t.kvh = r % p.Hkv;
+  t.b = r / p.Hkv;
+  t.q_start = t.b * p.q_len;
+  t.q0 = qb * p.QB;
+  t.nq = min(p.QB, p.q_len - t.q0);
+  t.k_start = p.cu_k[t.b];
+  t.Lk = p.cu_k[t.b + 1] - t.k_start;
+  t.pos0 = t.Lk - p.q_len + t.q0;
+  const int posN = t.pos0 + t.nq - 1;
+  const int chunk = (t.Lk + S - 1) / S;
+  t.k_lo = min(t.split * chunk, t.Lk);
+  t.k_hi = min(t.k_lo + chunk, t.Lk);
+  if (p.causal) t.k_hi = min(t.k_hi, posN + 1);
+  if (p.window > 0) t.k_lo = max(t.k_lo, t.pos0 - p.window + 1);
+  t.n = (t.k_hi > t.k_lo) ? (t.k_hi - t.k_lo + KT - 1) / KT : 0;
+  return t;
+}
+
 template <int RR>
 struct DtcCfg {
   static constexpr int D = 128;
   static constexpr int KT = 64;                 // keys per KV tile
-  static constexpr int NST = 3;                 // ring stages
   static constexpr int SUB_KV = KT * 128;       // [64 keys][64 bf16], 128B-swizzled: 8 KB
   static constexpr int KV_TILE = 2 * SUB_KV;    // K or V of one tile, d 128
   static constexpr int STAGE = 2 * KV_TILE;     // K and V: 32 KB
   static constexpr int Q_SUB = RR * 128;        // [RR rows][64 bf16]
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = (2 * Q_SUB + 1023) / 1024 * 1024;
-  static constexpr int OFF_BAR = OFF_RING + NST * STAGE;
-  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + 1;
-  static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
-  static constexpr int THREADS = 6 * 32;
-  static constexpr uint32_t TMEM_COLS = 256;
-  static constexpr uint32_t COL_O = 2 * KT;
+  static constexpr int Q_BUF = 2 * Q_SUB;       // one item's Q (two 64-column blocks)
   static constexpr int XS = D + 4;              // staging row stride (floats)
+  static constexpr int OFF_Q = 0;               // two Q buffers
+  static constexpr int OFF_RING = (2 * Q_BUF + 1023) / 1024 * 1024;
+  static constexpr int FIXED = OFF_RING + RR * XS * 4 + 2 * 128 * 16 + 40 * 8 + 64 + 1024;
+  static constexpr int NST = (232448 - FIXED) / STAGE < 6 ? (232448 - FIXED) / STAGE : 6;
+  static constexpr int OFF_STG = OFF_RING + NST * STAGE;   // [RR][XS] fp32 partial rows
+  static constexpr int OFF_ML = OFF_STG + RR * XS * 4;     // [2][128] (m, l, lr) per row
+  static constexpr int OFF_BAR = OFF_ML + 2 * 128 * 16;
+  static constexpr int NSB = 4;                 // S buffers in TMEM
+  static constexpr int N_BARS = 2 + 2 + 2 * NST + 3 * NSB + 2 + 2 + 2 + 1;
+  static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
+  static constexpr int THREADS = 12 * 32;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_O = NSB * KT;   // O buffers at 256 and 384
+  static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
   static_assert(RR % 8 == 0 && RR >= 8 && RR <= 128, "rows");
+  static_assert(NST >= 2, "ring depth");
   // the A operand reads 128 rows from each Q sub-tile: keep them inside the allocation
-  static_assert(OFF_Q + Q_SUB + 128 * 128 <= OFF_BAR, "Q over-read stays in shared memory");
-  static_assert(RR * XS * 4 <= NST * STAGE, "partial staging fits in the ring");
-  // at most two CTAs per SM, so two 256-column TMEM allocations always fit;
-  // up to 48 rows exactly two fit
-  static_assert(SMEM > 233472 / 3 - 1024 && SMEM <= 232448, "CTAs per SM");
-  static_assert(RR > 48 || 2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
+  static_assert(OFF_Q + Q_BUF + Q_SUB + 128 * 128 <= OFF_BAR, "Q over-read stays in shared memory");
+  // one CTA per SM, so the 512-column TMEM allocation always succeeds
+  static_assert(SMEM <= 232448 && 2 * (SMEM + 1024) > 233472, "one CTA per SM");
 };
 
+// Persistent: CTA c runs items c, c + gridDim.x, ... back to back, so the
+// ring keeps streaming across item boundaries. Warps 0-3 softmax (thread =
+// row = TMEM lane), 4-7 epilogue (read O, write the partial), 10 TMA
+// producer, 11 TMEM allocation + MMA issue (8, 9 idle: the producer and the
+// issuer sit on the SM sub-partitions of the softmax warps with the fewest
+// real rows). Q and O are double-buffered by item; S has four buffers: the
+// issuer keeps S three tiles ahead, issuing S(g+3) right after PV(g) (it
+// reuses P(g-1)'s buffer, whose PV has completed by then), so the chain
+// softmax -> PV -> S spans three tiles of softmax work.
+//
+// Lazy rescaling: a row's weights are taken relative to a reference maximum
+// that moves only when a score exceeds it by more than 2^8 in exp2 units,
+// so O is rarely rescaled (each rescale must wait for the previous PV) and
+// weights stay below 256. Two sums are kept: l over the exact weights and
+// lr over the bf16-rounded weights the MMA applies. The partial is written
+// as (m', lr) with m' = m + ln(l / lr): m' + ln lr is the chunk's exact
+// log-sum-exp and acc / lr its output normalised by the weights actually
+// applied -- the same state, rescaled, as (chunk max, exact sum).
 template <int RR>
-__global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 2)
+__global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const DtcParams p) {
@@ -92,58 +148,50 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = q_full + 1;
+  uint64_t* q_full = bars;              // [2] by non-empty item ordinal
+  uint64_t* q_empty = q_full + 2;       // [2] the item's last S has completed
+  uint64_t* kv_full = q_empty + 2;      // [NST] by tile ordinal
   uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;   // [2]: S(j) written to buffer j & 1
-  uint64_t* p_full = s_full + 2;       // [2]: P(j) written, O rescaled (128 arrivals)
-  uint64_t* pv_done = p_full + 2;      // [2]: PV(j) completed
-  uint64_t* drain = pv_done + 2;
+  uint64_t* s_full = kv_empty + NST;    // [4] S(g) in buffer g % 4
+  uint64_t* p_full = s_full + 4;        // [4] P(g) written and O rescaled (128 arrivals)
+  uint64_t* pv_done = p_full + 4;       // [4] PV(g) completed
+  uint64_t* o_full = pv_done + 4;       // [2] by item: its last PV has completed
+  uint64_t* o_free = o_full + 2;        // [2] by item: epilogue has read O and (m, l)
+  uint64_t* ml_full = o_free + 2;       // [2] by item: softmax wrote (m, l) (128 arrivals)
+  uint64_t* drain = ml_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float4* ml = reinterpret_cast<float4*>(smem + C::OFF_ML);
   int* status = &g_status_decode_tc;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.z;
-  const int kvh = blockIdx.y;
-  const int S = p.num_splits;
-  const int split = blockIdx.x % S;
-  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x / S);
-
-  const int q_start = b * p.q_len;
-  const int Lq = p.q_len;
-  const int k_start = p.cu_k[b];
-  const int Lk = p.cu_k[b + 1] - k_start;
-  const int q0 = qb * p.QB;
-  if (q0 >= Lq) return;   // uniform over the CTA, before any barrier or TMEM use
-  const int nq = min(p.QB, Lq - q0);
-  if (threadIdx.x == 0 && (Lk < Lq || Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
-  const int pos0 = Lk - Lq + q0;
-  const int posN = pos0 + nq - 1;
-  const int chunk = (Lk + S - 1) / S;
-  int k_lo = min(split * chunk, Lk);
-  int k_hi = min(k_lo + chunk, Lk);
-  if (p.causal) k_hi = min(k_hi, posN + 1);
-  if (p.window > 0) k_lo = max(k_lo, pos0 - p.window + 1);
-  const int n = (k_hi > k_lo) ? (k_hi - k_lo + KT - 1) / KT : 0;
+  const int n_mine = (p.n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                     static_cast<int>(gridDim.x);
+  auto item_of = [&](int k) { return dtc_item<KT>(p, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x)); };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 128);
+      mbar_init(&ml_full[i], 128);
+    }
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 11) {
     tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -151,235 +199,308 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+  };
 
-  if (warp == 4) {
+  if (warp == 10) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(2 * 128 * p.G * p.QB));
-      for (int sub = 0; sub < 2; ++sub)
-        tc::tma_load_3d(smem + C::OFF_Q + sub * C::Q_SUB, &tmQ, sub * 64, kvh * p.G,
-                        q_start + q0, q_full);
       const uint64_t policy = policy_evict_first();   // K/V are streamed once
-      const int slab = k_start * p.Hkv + kvh * Lk;     // tensor-map row of key 0
-      int issued = 0;
-      for (int i = 0; i < n; ++i) {
-        const int st = i % NST;
-        if (!mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1, abort_flag, status)) break;
-        uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
-        mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-        const int row = slab + k_hi - (n - i) * KT;
+      int g = 0, qi = 0;                               // tile and non-empty item ordinals
+      bool ok = true;
+      for (int k = 0; ok && k < n_mine; ++k) {
+        const DtcItem t = item_of(k);
+        if (t.Lk < p.q_len || t.Lk > p.max_kv) atomicExch(status, SINKATTN_BAD_LENGTHS);
+        if (t.n == 0) continue;
+        ok = mbar_wait(&q_empty[qi & 1], ((qi >> 1) & 1) ^ 1, abort_flag, status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&q_full[qi & 1], static_cast<uint32_t>(2 * 128 * p.G * p.QB));
+        for (int sub = 0; sub < 2; ++sub)
+          tc::tma_load_3d(smem + C::OFF_Q + (qi & 1) * C::Q_BUF + sub * C::Q_SUB, &tmQ, sub * 64,
+                          t.kvh * p.G, t.q_start + t.q0, &q_full[qi & 1]);
+        ++qi;
+        const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // tensor-map row of key 0
+        for (int j = 0; j < t.n; ++j, ++g) {
+          const int st = g % NST;
+          if (!mbar_wait(&kv_empty[st], ((g / NST) & 1) ^ 1, abort_flag, status)) { ok = false; break; }
+          uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
+          mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+          const int row = slab + t.k_hi - (t.n - j) * KT;
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          tma_load_2d_hint(kt + sub * C::SUB_KV, &tmK, sub * 64, row, &kv_full[st], policy);
-          tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV, &tmV, sub * 64, row, &kv_full[st],
-                           policy);
+          for (int sub = 0; sub < 2; ++sub) {
+            tma_load_2d_hint(kt + sub * C::SUB_KV, &tmK, sub * 64, row, &kv_full[st], policy);
+            tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV, &tmV, sub * 64, row, &kv_full[st],
+                             policy);
+          }
         }
-        issued = i + 1;
       }
       if (*abort_flag) {   // let every copy land before the CTA's shared memory goes away
-        mbar_drain(q_full, 0);
-        for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+        for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
+        for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 11) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
-      constexpr uint64_t STAGE16 = C::STAGE >> 4;   // descriptor address units
-      // A K step (16 elements = 32 bytes) inside a 128-byte swizzle row adds 2
-      // to the address field; the next 64-column block adds its sub-tile size.
-      const uint64_t qd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
-      const uint64_t kd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
-      // V as the MN-major B operand: d blocks of 64 one sub-tile apart, 8-key
-      // groups 1024 bytes apart; 16 keys advance 2048 bytes.
-      const uint64_t vd0 =
-          tc::smem_desc_sw128(smem_u32(smem + C::OFF_RING + C::KV_TILE), C::SUB_KV, 1024);
-      auto issue_s = [&](int j) {
-        const uint64_t kd = kd0 + static_cast<uint64_t>(j % NST) * STAGE16;
-        const uint32_t d_tm = tmem + static_cast<uint32_t>((j & 1) * KT);
+    // The whole warp runs the schedule (waits, cursors, descriptor arithmetic
+    // stay warp-uniform) and one elected lane issues each MMA and commit.
+    const bool leader = tc::elect_one();
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
+    constexpr uint64_t STAGE16 = C::STAGE >> 4;   // descriptor address units
+    // A K step (16 elements = 32 bytes) inside a 128-byte swizzle row adds 2
+    // to the address field; the next 64-column block adds its sub-tile size.
+    const uint64_t qd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t kd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+    // V as the MN-major B operand: d blocks of 64 one sub-tile apart, 8-key
+    // groups 1024 bytes apart; 16 keys advance 2048 bytes.
+    const uint64_t vd0 =
+        tc::smem_desc_sw128(smem_u32(smem + C::OFF_RING + C::KV_TILE), C::SUB_KV, 1024);
+
+    // S cursor: runs three tiles ahead of the PV cursor (four S buffers).
+    int sk = 0, sj = 0, sg = 0, sqi = 0;
+    DtcItem st_ = n_mine > 0 ? item_of(0) : DtcItem{};
+    auto s_skip_empty = [&]() {
+      while (sk < n_mine && st_.n == 0) {
+        ++sk;
+        if (sk < n_mine) st_ = item_of(sk);
+      }
+    };
+    auto issue_next_s = [&]() -> bool {
+      if (sj == 0 && !wwait(&q_full[sqi & 1], (sqi >> 1) & 1)) return false;
+      if (!wwait(&kv_full[sg % NST], (sg / NST) & 1)) return false;
+      // S(sg) overwrites P(sg - 4): PV(sg - 4) must have read it
+      if (sg >= 4 && !wwait(&pv_done[sg & 3], ((sg - 4) >> 2) & 1)) return false;
+      tc::fence_after_sync();
+      const uint64_t qd = qd0 + static_cast<uint64_t>(sqi & 1) * (C::Q_BUF >> 4);
+      const uint64_t kd = kd0 + static_cast<uint64_t>(sg % NST) * STAGE16;
+      const uint32_t d_tm = tmem + static_cast<uint32_t>((sg & 3) * KT);
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t oq = static_cast<uint64_t>(kk >> 2) * (C::Q_SUB >> 4) + (kk & 3) * 2;
           const uint64_t ok = static_cast<uint64_t>(kk >> 2) * (C::SUB_KV >> 4) + (kk & 3) * 2;
-          tc::mma_ss(d_tm, qd0 + oq, kd + ok, idesc_s, kk > 0 ? 1u : 0u);
+          tc::mma_ss(d_tm, qd + oq, kd + ok, idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc::commit(&s_full[j & 1]);
-      };
-      auto issue_pv = [&](int j) {
-        const uint64_t vd = vd0 + static_cast<uint64_t>(j % NST) * STAGE16;
-        const uint32_t a_tm = tmem + static_cast<uint32_t>((j & 1) * KT);
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk)
-          tc::mma_ts(tmem + C::COL_O, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u,
-                     idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&pv_done[j & 1]);
-        tc::commit(&kv_empty[j % NST]);
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, status);
-      for (int j = 0; ok && j < min(n, 2); ++j) {
-        ok = mbar_wait(&kv_full[j], 0, abort_flag, status);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_s(j);
-        }
+        tc::commit(&s_full[sg & 3]);
       }
-      for (int j = 0; ok && j < n; ++j) {
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, status)) break;
+      __syncwarp();
+      ++sg;
+      if (++sj == st_.n) {   // the item's last S: its Q buffer frees when this completes
+        if (leader) tc::commit(&q_empty[sqi & 1]);
+        __syncwarp();
+        ++sqi;
+        sj = 0;
+        ++sk;
+        if (sk < n_mine) st_ = item_of(sk);
+        s_skip_empty();
+      }
+      return true;
+    };
+
+    bool ok = true;
+    s_skip_empty();
+    for (int w = 0; w < 3 && ok && sk < n_mine; ++w) ok = issue_next_s();
+    int g = 0;   // PV cursor: tile ordinal
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const int n = item_of(k).n;
+      // O buffer k & 1 is reused: the epilogue of item k - 2 has read it
+      if (k >= 2 && !wwait(&o_free[k & 1], ((k - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t o_tm = tmem + C::COL_O + static_cast<uint32_t>((k & 1) * D);
+      for (int j = 0; j < n; ++j, ++g) {
+        if (!wwait(&p_full[g & 3], (g >> 2) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_pv(j);
-        if (j + 2 < n) {
-          // S(j+2) overwrites P(j): wait until PV(j) has read it.
-          if (!mbar_wait(&kv_full[(j + 2) % NST], ((j + 2) / NST) & 1, abort_flag, status) ||
-              !mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag, status))
-            break;
-          tc::fence_after_sync();
-          issue_s(j + 2);
+        const uint64_t vd = vd0 + static_cast<uint64_t>(g % NST) * STAGE16;
+        const uint32_t a_tm = tmem + static_cast<uint32_t>((g & 3) * KT);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk)
+            tc::mma_ts(o_tm, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u, idesc_o,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&pv_done[g & 3]);
+          tc::commit(&kv_empty[g % NST]);
         }
+        __syncwarp();
+        // S(g+3) into P(g-1)'s buffer: PV(g-1) was issued a tile ago
+        if (sk < n_mine && !issue_next_s()) { ok = false; break; }
       }
-      // every MMA this thread issued has completed before the CTA frees TMEM
-      tc::commit(drain);
-      mbar_drain(drain, 0);
+      if (!ok) break;
+      if (leader) tc::commit(&o_full[k & 1]);   // also for an empty item: nothing to wait for
+      __syncwarp();
     }
-  } else {
+    // every MMA this warp issued has completed before the CTA frees TMEM
+    if (leader) tc::commit(drain);
+    __syncwarp();
+    mbar_drain(drain, 0);
+  } else if (warp < 4) {
     // ---------------------------------------------------------------- softmax
     const int row = warp * 32 + lane;   // TMEM lane; warp w owns lanes 32w..32w+31
     const int G = p.G;
     const int tl = row / G;
-    const bool valid = tl < nq;
-    const int pos = pos0 + tl;
-    int lo_r = k_lo, hi_r = k_hi - 1;
-    if (p.window > 0) lo_r = max(lo_r, pos - p.window + 1);
-    if (p.causal) hi_r = min(hi_r, pos);
-    if (!valid) {   // padding lanes see no key: P = 0
-      lo_r = 1;
-      hi_r = 0;
-    }
+    const bool warp_rows = warp * 32 < p.G * p.QB;   // the warp holds a real row of some item
     const float c2 = p.scale_log2;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t o_addr = lane_base + C::COL_O;
-    float m = NEG_INF, l = 0.f;   // running max (raw logits) and exact sum
     bool ok = true;
-    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
-    };
-
-    for (int j = 0; j < n; ++j) {
-      if (!wwait(&s_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
-      tc::fence_after_sync();
-      const uint32_t s_addr = lane_base + static_cast<uint32_t>((j & 1) * KT);
-      const int j0 = k_hi - (n - j) * KT;   // key of tile column 0
-      float v[2][32];
-      tc::tmem_ld32(s_addr, v[0]);
-      tc::tmem_ld32(s_addr + 32, v[1]);
-      tc::tmem_wait_ld();
-      if (j0 < lo_r || j0 + KT - 1 > hi_r) {
-        const int clo = lo_r - j0, chi = hi_r - j0;
+    int g = 0;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const DtcItem t = item_of(k);
+      const bool valid = tl < t.nq;
+      const int pos = t.pos0 + tl;
+      int lo_r = t.k_lo, hi_r = t.k_hi - 1;
+      if (p.window > 0) lo_r = max(lo_r, pos - p.window + 1);
+      if (p.causal) hi_r = min(hi_r, pos);
+      const uint32_t o_addr = lane_base + C::COL_O + static_cast<uint32_t>((k & 1) * D);
+      // reference maximum (raw logits), exact and rounded weight sums
+      float m = NEG_INF, l = 0.f, lr = 0.f;
+      for (int j = 0; j < t.n; ++j, ++g) {
+        if (!wwait(&s_full[g & 3], (g >> 2) & 1)) { ok = false; break; }
+        if (!warp_rows) {   // padding rows only: nothing to compute, keep the barriers' count
+          mbar_arrive(&p_full[g & 3]);
+          continue;
+        }
+        tc::fence_after_sync();
+        const uint32_t s_addr = lane_base + static_cast<uint32_t>((g & 3) * KT);
+        const int j0 = t.k_hi - (t.n - j) * KT;   // key of tile column 0
+        float v[2][32];
+        tc::tmem_ld32(s_addr, v[0]);
+        tc::tmem_ld32(s_addr + 32, v[1]);
+        tc::tmem_wait_ld();
+        // (padding lanes skip the mask: their weights are zeroed below)
+        if (valid && (j0 < lo_r || j0 + KT - 1 > hi_r)) {
+          const int clo = lo_r - j0, chi = hi_r - j0;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e < clo || c * 32 + e > chi) v[c][e] = NEG_INF;
+        }
+        float mx4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < clo || c * 32 + e > chi) v[c][e] = NEG_INF;
-      }
-      float mx4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], v[c][e]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mx > m) {
-        alpha = (m == NEG_INF) ? 0.f : ex2((m - mx) * c2);
-        m = mx;
-        rescale = true;
-      }
-      const float mb = (m == NEG_INF) ? 0.f : m * c2;
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a0 = ex2(fmaf(v[c][e], c2, -mb));
-          const float a1 = ex2(fmaf(v[c][e + 1], c2, -mb));
-          rs4[(e >> 1) & 3] += a0 + a1;
-          pk[e >> 1] = pack_bf16x2(a0, a1);
+          for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], v[c][e]);
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float alpha = 1.f;
+        bool rescale = false;
+        if (valid && (m == NEG_INF ? mx > m : (mx - m) * c2 > 8.f)) {
+          alpha = (m == NEG_INF) ? 0.f : ex2((m - mx) * c2);
+          m = mx;
+          rescale = true;
         }
-        // P columns [16c, 16c + 16) hold scores this thread already loaded
-        tc::tmem_st16(s_addr + 16 * c, pk);
-      }
-      // O rescale (PV(j-1) must have completed; warp-uniform branch)
-      if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-        if (!wwait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
+        // padding lanes: an infinite offset makes every weight 0 (their S rows
+        // are garbage; only their own P and O rows see it)
+        const float mb = !valid ? INFINITY : (m == NEG_INF) ? 0.f : m * c2;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float a0 = ex2(fmaf(v[c][e], c2, -mb));
+            const float a1 = ex2(fmaf(v[c][e + 1], c2, -mb));
+            rs4[(e >> 1) & 3] += a0 + a1;
+            pk[e >> 1] = pack_bf16x2(a0, a1);
+            rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+          }
+          // P columns [16c, 16c + 16) hold scores this thread already loaded
+          tc::tmem_st16(s_addr + 16 * c, pk);
+        }
+        // O rescale (rare): PV(g - 1) of this item must have completed; warp-uniform
+        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+          if (!wwait(&pv_done[(g - 1) & 3], ((g - 1) >> 2) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc::tmem_ld32(o_addr + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tc::tmem_st32(o_addr + c * 32, o);
+          }
+        }
+        tc::tmem_wait_st();
+        l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+        lr = lr * alpha + ((rr4[0] + rr4[1]) + (rr4[2] + rr4[3]));
+        tc::fence_before_sync();
+        mbar_arrive(&p_full[g & 3]);
+      }
+      if (!ok) break;
+      // hand (m, l) to the epilogue once it is done with item k - 2's
+      if (k >= 2 && !wwait(&o_free[k & 1], ((k - 2) >> 1) & 1)) { ok = false; break; }
+      ml[(k & 1) * 128 + row] = make_float4(m, l, lr, 0.f);
+      mbar_arrive(&ml_full[k & 1]);
+    }
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp - 4;
+    const int row = quad * 32 + lane;
+    const int G = p.G;
+    const int tl = row / G;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_STG);
+    const int S = p.num_splits;
+    for (int k = 0; k < n_mine; ++k) {
+      const DtcItem t = item_of(k);
+      if (!wwait(&o_full[k & 1], (k >> 1) & 1) || !wwait(&ml_full[k & 1], (k >> 1) & 1)) break;
+      tc::fence_after_sync();
+      const float4 mlr = ml[(k & 1) * 128 + row];
+      const uint32_t o_addr = lane_base + C::COL_O + static_cast<uint32_t>((k & 1) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (t.n >= 1) {
           tc::tmem_ld32(o_addr + c * 32, o);
           tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc::tmem_st32(o_addr + c * 32, o);
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (row < RR) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(stage + row * C::XS + c * 32 + e) =
+                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
       }
-      tc::tmem_wait_st();
-      l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
       tc::fence_before_sync();
-      mbar_arrive(&p_full[j & 1]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (ok && n >= 1) {
-      ok = wwait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
-      tc::fence_after_sync();
-    }
-    // Every tile has been consumed and every PV has completed: the ring is
-    // free and stages this CTA's partial rows for coalesced stores.
-    float* stage = reinterpret_cast<float*>(smem + C::OFF_RING);
-    const bool have_o = ok && n >= 1;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      float o[32];
-      if (have_o) {
-        tc::tmem_ld32(o_addr + c * 32, o);
-        tc::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      mbar_arrive(&o_free[k & 1]);
+      if (tl < t.nq) {
+        const size_t rowid =
+            static_cast<size_t>(t.q_start + t.q0 + tl) * p.Hq + t.kvh * G + (row - tl * G);
+        // (m', lr): m' + ln lr = m + ln l, the chunk's exact log-sum-exp
+        float2 md;
+        if (mlr.x == NEG_INF || !(mlr.z > 0.f)) {
+          md = make_float2(NEG_INF, 0.f);
+        } else {
+          md.x = mlr.x * p.sm_scale + (lg2(mlr.y) - lg2(mlr.z)) * kLn2;
+          md.y = mlr.z;
+        }
+        *reinterpret_cast<float2*>(p.part_md + (rowid * S + t.split) * 2) = md;
       }
-      if (row < RR) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(stage + row * C::XS + c * 32 + e) =
-              make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+      named_barrier_sync(1, 128);   // staging written
+      const int nrows = t.nq * G;
+      for (int r = quad; r < nrows; r += 4) {
+        const int t2 = r / G;
+        const size_t rowid =
+            static_cast<size_t>(t.q_start + t.q0 + t2) * p.Hq + t.kvh * G + (r - t2 * G);
+        const float4 val = *reinterpret_cast<const float4*>(stage + r * C::XS + lane * 4);
+        *reinterpret_cast<float4*>(p.part_acc + (rowid * S + t.split) * D + lane * 4) = val;
       }
-    }
-    if (valid) {
-      const size_t rowid =
-          static_cast<size_t>(q_start + q0 + tl) * p.Hq + kvh * G + (row - tl * G);
-      float2 md;
-      md.x = (m == NEG_INF) ? NEG_INF : m * p.sm_scale;
-      md.y = l;
-      *reinterpret_cast<float2*>(p.part_md + (rowid * S + split) * 2) = md;
-    }
-    named_barrier_sync(1, 128);
-    const int nrows = nq * G;
-    for (int r = warp; r < nrows; r += 4) {
-      const int t2 = r / G;
-      const size_t rowid = static_cast<size_t>(q_start + q0 + t2) * p.Hq + kvh * G + (r - t2 * G);
-      const float4 val = *reinterpret_cast<const float4*>(stage + r * C::XS + lane * 4);
-      *reinterpret_cast<float4*>(p.part_acc + (rowid * S + split) * D + lane * 4) = val;
+      named_barrier_sync(1, 128);   // staging read before the next item overwrites it
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 11) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -407,6 +528,12 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
   p.QB = QB;
   p.nqb = (a.q_len + QB - 1) / QB;
   p.num_splits = a.num_splits;
+  const int64_t items = static_cast<int64_t>(a.batch) * a.Hkv * p.nqb * a.num_splits;
+  if (items >= (int64_t{1} << 31)) {
+    set_error("too many work items");
+    return SINKATTN_UNSUPPORTED;
+  }
+  p.n_items = static_cast<int>(items);
   p.max_kv = a.max_kv;
   p.sm_scale = a.sm_scale;
   p.scale_log2 = a.sm_scale * kLog2e;
@@ -420,8 +547,8 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     return SINKATTN_CUDA_ERROR;
   }
-  const dim3 grid(static_cast<unsigned>(p.nqb * p.num_splits), static_cast<unsigned>(a.Hkv),
-                  static_cast<unsigned>(a.batch));
+  if (p.n_items == 0) return SINKATTN_OK;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, sm_count()));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmQ, tmK, tmV, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -106,10 +106,17 @@ SINKATTN_API int sinkattn_prefill(const void* q, const void* k, const void* v, c
  *   max_kv_len bounds every Lk_b (host); each sequence needs Lk_b >= q_len.
  *   Sequence b's keys are cut into num_splits chunks of c = ceil(Lk_b/num_splits)
  *   keys; chunk s covers [s*c, min((s+1)*c, Lk_b)) and may be empty.
- *   part_acc: fp32 [batch*q_len, Hq, num_splits, d]: sum_j e^{l_j - m_s} v_j;
- *   part_md:  fp32 [batch*q_len, Hq, num_splits, 2]: (m_s, d_s) with m_s the
- *             largest visible logit of the chunk (natural units) and
- *             d_s = sum_j e^{l_j - m_s}; an empty chunk gives (-inf, 0) and acc 0.
+ *   part_md:  fp32 [batch*q_len, Hq, num_splits, 2]: (m_s, d_s), natural
+ *             units, with m_s + ln d_s = ln sum_j e^{l_j}, the chunk's
+ *             log-sum-exp over its visible keys;
+ *   part_acc: fp32 [batch*q_len, Hq, num_splits, d]: d_s times the chunk's
+ *             softmax-weighted mean of v_j, i.e. sum_j e^{l_j - m_s} v_j.
+ *   The pair is defined up to the common rescale (m_s + c, d_s e^{-c},
+ *   acc e^{-c}), which the merge is invariant to. The warp-level kernel
+ *   writes m_s = the chunk's largest visible logit and d_s = the exact sum;
+ *   the tcgen05 kernel writes d_s = the sum of the bf16-rounded weights its
+ *   P.V product applied, with m_s adjusted so that m_s + ln d_s stays exact.
+ *   An empty chunk gives (-inf, 0) and acc 0.
  */
 SINKATTN_API int sinkattn_decode_split(const void* q, const void* k, const void* v,
                           const int32_t* kv_indptr, int32_t batch, int32_t q_len,

@@ -326,6 +326,26 @@ def test_ceil_split_rule_then_merge_equals_unsplit(oracle_lib, S):
         assert np.isfinite(m[tok, 0]).sum() == n_nonempty
 
 
+def test_merge_is_invariant_to_rescaled_partials(oracle_lib):
+    """A chunk's partial (m, d, acc) is a softmax state up to a common scale:
+    (m + c, d e^-c, acc e^-c) describes the same chunk, so the merge must give
+    the same out and lse for any c per (row, head, chunk)."""
+    Hq, Hkv, d = 6, 2, 8
+    inp = workloads.explicit_inputs([2, 3], [40, 25], Hq, Hkv, d, seed=14)
+    sinks = np.linspace(-1, 3, Hq)
+    acc, m, dd = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"], Hq,
+                                       Hkv, d, 0.3, True, 0, 5)
+    out, lse = oracle.merge(acc, m, dd, sinks, Hq, d)
+    c = np.random.default_rng(3).uniform(-6, 6, size=m.shape)
+    fin = np.isfinite(m)
+    m2 = np.where(fin, m + c, m)
+    d2 = np.where(fin, dd * np.exp(-c), dd)
+    acc2 = np.where(fin[..., None], acc * np.exp(-c)[..., None], acc)
+    out2, lse2 = oracle.merge(acc2, m2, d2, sinks, Hq, d)
+    np.testing.assert_allclose(out2, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+
+
 # --------------------------------------------------------------------------
 # second implementation (exactly rounded sums)
 # --------------------------------------------------------------------------

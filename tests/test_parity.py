@@ -98,6 +98,24 @@ def test_tiny_workload_prefill_and_decode():
         compare(out, lse, want_out, want_lse, "tiny decode S=%d" % S)
 
 
+def check_partials(acc, md, acc_o, m_o, d_o):
+    """Split partials against the oracle's. A partial (m, d, acc) is defined
+    up to a common rescale, so compare what is unique: which chunks are
+    empty, the chunk's log-sum-exp m + ln d, and its normalised output acc / d."""
+    acc_g, md_g = acc.cpu().numpy(), md.cpu().numpy()
+    m_g, d_g = md_g[..., 0], md_g[..., 1]
+    empty = np.isneginf(m_o)
+    assert (np.isneginf(m_g) == empty).all()
+    assert (d_g[empty] == 0).all() and (acc_g[empty] == 0).all()
+    ne = ~empty
+    lse_g = m_g[ne] + np.log(d_g[ne])
+    lse_o = m_o[ne] + np.log(d_o[ne])
+    assert np.abs(lse_g - lse_o).max() <= TOL_LSE
+    og = acc_g[ne] / d_g[ne][:, None]
+    oo = acc_o[ne] / d_o[ne][:, None]
+    assert np.abs(og - oo).max() <= TOL_MAX and np.abs(og - oo).mean() <= TOL_MEAN
+
+
 def _decode_inputs(B, q_len, Hq, Hkv, d, kv_range, seed, q_scale=1.0):
     w = workloads.Workload("t", "decode", Hq, Hkv, d, True, batch=B, q_len=q_len,
                            kv_range=kv_range, sink_dist="uniform2", seed=seed)
@@ -144,17 +162,7 @@ def _decode_split_merge(case):
     torch.cuda.synchronize()
     acc_o, m_o, d_o = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"],
                                             Hq, Hkv, d, scale, True, window, S)
-    acc_g, md_g = acc.cpu().numpy(), md.cpu().numpy()
-    m_g, d_g = md_g[..., 0], md_g[..., 1]
-    empty = np.isneginf(m_o)
-    assert (np.isneginf(m_g) == empty).all()
-    assert (d_g[empty] == 0).all() and (acc_g[empty] == 0).all()
-    ne = ~empty
-    assert np.abs(m_g[ne] - m_o[ne]).max() <= TOL_LSE
-    assert np.abs(np.log(d_g[ne]) - np.log(d_o[ne])).max() <= TOL_LSE
-    og = acc_g[ne] / d_g[ne][:, None]
-    oo = acc_o[ne] / d_o[ne][:, None]
-    assert np.abs(og - oo).max() <= TOL_MAX and np.abs(og - oo).mean() <= TOL_MEAN
+    check_partials(acc, md, acc_o, m_o, d_o)
 
     # step 2: the merge alone, fed the oracle's partials
     mo, lo = oracle.merge(acc_o, m_o, d_o, inp["sinks"], Hq, d)
@@ -171,6 +179,29 @@ def _decode_split_merge(case):
                                   Hkv, num_splits=S, sm_scale=scale, window=window)
     torch.cuda.synchronize()
     compare(out, lse, want_out, want_lse, "decode")
+
+
+def test_merge_accepts_rescaled_partials():
+    """sinkattn_merge reads a partial only through the invariant m + ln d and
+    acc / d: the oracle's partials rescaled by a random c per chunk give the
+    oracle's unsplit result."""
+    B, q_len, Hq, Hkv, d, S = 3, 3, 32, 2, 128, 6
+    inp = _decode_inputs(B, q_len, Hq, Hkv, d, (3, 700), seed=91)
+    scale = 1.0 / math.sqrt(d)
+    acc_o, m_o, d_o = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"],
+                                            Hq, Hkv, d, scale, True, 0, S)
+    c = np.random.default_rng(5).uniform(-10, 10, size=m_o.shape)
+    fin = np.isfinite(m_o)
+    m2 = np.where(fin, m_o + c, m_o)
+    d2 = np.where(fin, d_o * np.exp(-c), d_o)
+    acc2 = np.where(fin[..., None], acc_o * np.exp(-c)[..., None], acc_o)
+    part_acc = torch.from_numpy(acc2.astype(np.float32)).cuda()
+    part_md = torch.from_numpy(np.stack([m2, d2], -1).astype(np.float32)).cuda()
+    out, lse = sa.sinkattn_merge(part_acc, part_md, inp["sinks"].cuda())
+    torch.cuda.synchronize()
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, True, 0)
+    compare(out, lse, want_out, want_lse, "merge of rescaled partials")
 
 
 TC_DECODE_CASES = [
@@ -205,17 +236,7 @@ def test_tcgen05_decode_partials(case):
         sa.sinkattn_set_decode_kernel("auto")
     acc_o, m_o, d_o = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"],
                                             Hq, Hkv, d, scale, True, window, S)
-    acc_g, md_g = acc.cpu().numpy(), md.cpu().numpy()
-    m_g, d_g = md_g[..., 0], md_g[..., 1]
-    empty = np.isneginf(m_o)
-    assert (np.isneginf(m_g) == empty).all()
-    assert (d_g[empty] == 0).all() and (acc_g[empty] == 0).all()
-    ne = ~empty
-    assert np.abs(m_g[ne] - m_o[ne]).max() <= TOL_LSE
-    assert np.abs(np.log(d_g[ne]) - np.log(d_o[ne])).max() <= TOL_LSE
-    og = acc_g[ne] / d_g[ne][:, None]
-    oo = acc_o[ne] / d_o[ne][:, None]
-    assert np.abs(og - oo).max() <= TOL_MAX and np.abs(og - oo).mean() <= TOL_MEAN
+    check_partials(acc, md, acc_o, m_o, d_o)
     want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
                                        inp["cu_k"], Hq, Hkv, d, scale, True, window)
     compare(out, lse, want_out, want_lse, "tcgen05 decode")
