@@ -13,7 +13,8 @@
 //  * warp 0: TMA producer (Q_A and Q_B once as 3-D boxes, then K/V tiles of
 //    128 keys into an NST-stage ring, right-aligned to the end of the key
 //    range so no copy reads past the last key needed);
-//  * warp 1: allocates TMEM and issues every MMA from one thread, ping-ponging
+//  * warp 1: allocates TMEM and issues every MMA from one elected lane (the
+//    warp runs the schedule uniformly), ping-ponging
 //    the two tiles so the tensor core works on one while the other's softmax
 //    runs:  S_A(0), S_B(0), then per KV tile j:
 //           PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
@@ -199,7 +200,13 @@ __global__ void __launch_bounds__(576, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule (waits and descriptor arithmetic stay
+    // warp-uniform); one elected lane issues each MMA and commit.
+    const bool leader = tc::elect_one();
+    auto wwait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+    };
+    {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, C::NO, true);
       constexpr uint64_t STAGE16 = C::STAGE >> 4;   // one K/V stage, in descriptor address units
@@ -219,12 +226,15 @@ __global__ void __launch_bounds__(576, 1)
         const uint64_t kd = kd0 + static_cast<uint64_t>(j % NST) * STAGE16;
         const uint64_t qd = qd0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
         const uint32_t d_tm = tmem + C::col_s(t);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = static_cast<uint64_t>(kk >> 2) * SUB16 + static_cast<uint64_t>(kk & 3) * 2;
-          tc::mma_ss(d_tm, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(kk >> 2) * SUB16 + static_cast<uint64_t>(kk & 3) * 2;
+            tc::mma_ss(d_tm, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc::commit(&s_full[t]);
         }
-        tc::commit(&s_full[t]);
+        __syncwarp();
       };
       auto issue_pv = [&](int t, int j) {
         const uint64_t st = static_cast<uint64_t>(j % NST);
@@ -232,15 +242,18 @@ __global__ void __launch_bounds__(576, 1)
                                       : vd0 + st * STAGE16;
         const uint32_t d_tm = tmem + C::col_o(t);
         const uint32_t a_tm = tmem + C::col_s(t);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk)
-          tc::mma_ts(d_tm, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u, idesc_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&pv_done[t]);
+          for (int kk = 0; kk < KT / 16; ++kk)
+            tc::mma_ts(d_tm, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u, idesc_o,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&pv_done[t]);
+        }
+        __syncwarp();
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, status);
+      bool ok = wwait1(q_full, 0);
       if (ok && n > 0) {
-        ok = mbar_wait(&kv_full[0], 0, abort_flag, status);
+        ok = wwait1(&kv_full[0], 0);
         if (ok) {
           tc::fence_after_sync();
           issue_s(0, 0);
@@ -249,21 +262,25 @@ __global__ void __launch_bounds__(576, 1)
       }
       for (int j = 0; ok && j < n; ++j) {
         for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait(&p_full[t], j & 1, abort_flag, status)) { ok = false; break; }
+          if (!wwait1(&p_full[t], j & 1)) { ok = false; break; }
           tc::fence_after_sync();
           issue_pv(t, j);
-          if (t == 1) tc::commit(&kv_empty[j % NST]);
+          if (t == 1) {
+            if (leader) tc::commit(&kv_empty[j % NST]);
+            __syncwarp();
+          }
           if (j + 1 < n) {
-            if (t == 0 && !mbar_wait(&kv_full[(j + 1) % NST], ((j + 1) / NST) & 1, abort_flag, status)) { ok = false; break; }
+            if (t == 0 && !wwait1(&kv_full[(j + 1) % NST], ((j + 1) / NST) & 1)) { ok = false; break; }
             // S_t(j+1) overwrites P_t(j): wait until PV_t(j) has read it.
-            if (!mbar_wait(&pv_done[t], j & 1, abort_flag, status)) { ok = false; break; }
+            if (!wwait1(&pv_done[t], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
             issue_s(t, j + 1);
           }
         }
       }
-      // every MMA this thread issued has completed before the CTA frees TMEM
-      tc::commit(drain);
+      // every MMA this warp issued has completed before the CTA frees TMEM
+      if (leader) tc::commit(drain);
+      __syncwarp();
       mbar_drain(drain, 0);
     }
   } else {
