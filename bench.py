@@ -168,42 +168,38 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
     for _ in range(warmup):
         run()
     split_ms = None
+    # the step: `steps` calls back to back (for decode the merge is launched
+    # as a programmatic dependent of the partial kernel, so nothing may sit
+    # between them on the stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _sync(dist_ctx)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    _sync(dist_ctx)
+    ms = e0.elapsed_time(e1) / steps
     if w.kind == "decode" and want_kernel_split and not run.fused:
-        # split and merge launched separately with an event between them, so
-        # the dominant kernel's own time is measured inside the timed region
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
-        part_acc = run.workspace[: 0]
+        # the dominant kernel's own time: the same partial launches back to
+        # back, bracketed by events on the launching stream
         n_acc = inp["total_q"] * w.num_qo_heads * run.num_splits * w.head_dim * 4
         off = (n_acc + 255) // 256 * 256
         acc = run.workspace[:n_acc].view(torch.float32).view(inp["total_q"], w.num_qo_heads,
                                                             run.num_splits, w.head_dim)
         md = run.workspace[off: off + inp["total_q"] * w.num_qo_heads * run.num_splits * 8].view(
             torch.float32).view(inp["total_q"], w.num_qo_heads, run.num_splits, 2)
-        del part_acc
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         _sync(dist_ctx)
-        evs[0].record(stream)
-        for i in range(steps):
+        s0.record(stream)
+        for _ in range(steps):
             B.sinkattn_decode_split(inp["q"], inp["k"], inp["v"], inp["cu_k"], w.q_len, inp["max_k"],
                                     w.num_kv_heads, run.num_splits, w.scale, w.causal, w.window,
                                     part_acc=acc, part_md=md)
-            evs[2 * i + 1].record(stream)
-            B.sinkattn_merge(acc, md, inp["sinks"], out=run.out, lse=run.lse)
-            evs[2 * i + 2].record(stream)
+        s1.record(stream)
         _sync(dist_ctx)
-        total = evs[0].elapsed_time(evs[-1])
-        split_ms = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(steps)) / steps
-        ms = total / steps
-    else:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        _sync(dist_ctx)
-        e0.record(stream)
-        for _ in range(steps):
-            run()
-        e1.record(stream)
-        _sync(dist_ctx)
-        ms = e0.elapsed_time(e1) / steps
-        if w.kind == "decode":
-            split_ms = ms   # the fused kernel is the whole step
+        split_ms = s0.elapsed_time(s1) / steps
+    elif w.kind == "decode":
+        split_ms = ms   # the fused kernel is the whole step
     ms = _max_over_ranks(ms, dist_ctx)
     if split_ms is not None:
         split_ms = _max_over_ranks(split_ms, dist_ctx)

@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
     }
     cluster_sync_all();   // peers may still be reading this CTA's partial
   }
+  // split mode: this thread's partial writes are issued; a dependent merge
+  // may start launching (it waits for the whole grid before reading)
+  if (!FUSED) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

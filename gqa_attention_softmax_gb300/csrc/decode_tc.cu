@@ -46,6 +46,7 @@ __device__ int g_status_decode_tc;
 
 struct DtcParams {
   const int32_t* cu_k;
+  int batch;
   int q_len, Hq, Hkv, G, QB, nqb, num_splits, max_kv;
   int n_items;   // batch * Hkv * nqb * num_splits
   float sm_scale, scale_log2;
@@ -59,8 +60,10 @@ struct DtcItem {
   int b, kvh, split, q_start, q0, nq, k_start, Lk, pos0, k_lo, k_hi, n;
 };
 
+// cu_k is read from `cu` (a shared-memory copy when the batch fits, else
+// global memory): every role derives every item's keys from it.
 template <int KT>
-__device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, int it) {
+__device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* cu, int it) {
   DtcItem t;
   const int S = p.num_splits;
   t.split = it % S;
@@ -72,8 +75,8 @@ __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, int it) {
   t.q_start = t.b * p.q_len;
   t.q0 = qb * p.QB;
   t.nq = min(p.QB, p.q_len - t.q0);
-  t.k_start = p.cu_k[t.b];
-  t.Lk = p.cu_k[t.b + 1] - t.k_start;
+  t.k_start = cu[t.b];
+  t.Lk = cu[t.b + 1] - t.k_start;
   t.pos0 = t.Lk - p.q_len + t.q0;
   const int posN = t.pos0 + t.nq - 1;
   const int chunk = (t.Lk + S - 1) / S;
@@ -97,11 +100,14 @@ struct DtcCfg {
   static constexpr int XS = D + 4;              // staging row stride (floats)
   static constexpr int OFF_Q = 0;               // two Q buffers
   static constexpr int OFF_RING = (2 * Q_BUF + 1023) / 1024 * 1024;
-  static constexpr int FIXED = OFF_RING + RR * XS * 4 + 2 * 128 * 16 + 40 * 8 + 64 + 1024;
+  static constexpr int CU_CAP = 2048;           // sequences whose kv_indptr is staged in smem
+  static constexpr int FIXED =
+      OFF_RING + RR * XS * 4 + 2 * 128 * 16 + (CU_CAP + 1) * 4 + 16 + 40 * 8 + 64 + 1024;
   static constexpr int NST = (232448 - FIXED) / STAGE < 6 ? (232448 - FIXED) / STAGE : 6;
   static constexpr int OFF_STG = OFF_RING + NST * STAGE;   // [RR][XS] fp32 partial rows
   static constexpr int OFF_ML = OFF_STG + RR * XS * 4;     // [2][128] (m, l, lr) per row
-  static constexpr int OFF_BAR = OFF_ML + 2 * 128 * 16;
+  static constexpr int OFF_CU = OFF_ML + 2 * 128 * 16;     // [CU_CAP + 1] kv_indptr copy
+  static constexpr int OFF_BAR = OFF_CU + ((CU_CAP + 1) * 4 + 15) / 16 * 16;
   static constexpr int NSB = 4;                 // S buffers in TMEM
   static constexpr int N_BARS = 2 + 2 + 2 * NST + 3 * NSB + 2 + 2 + 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
@@ -168,7 +174,17 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int n_mine = (p.n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                      static_cast<int>(gridDim.x);
-  auto item_of = [&](int k) { return dtc_item<KT>(p, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x)); };
+  // kv_indptr in shared memory (global-memory loads under a saturated HBM
+  // stream take microseconds, and every role needs every item's keys)
+  int32_t* cu_s = reinterpret_cast<int32_t*>(smem + C::OFF_CU);
+  const int n_cu = p.batch + 1;
+  const bool cu_in_smem = n_cu <= C::CU_CAP + 1;
+  if (cu_in_smem)
+    for (int i = threadIdx.x; i < n_cu; i += blockDim.x) cu_s[i] = p.cu_k[i];
+  const int32_t* cu = cu_in_smem ? cu_s : p.cu_k;
+  auto item_of = [&](int k) {
+    return dtc_item<KT>(p, cu, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x));
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 4; ++i) {
@@ -500,6 +516,8 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
 
   tc::fence_before_sync();
   __syncthreads();
+  // this CTA's partials are written: a dependent merge may start launching
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 11) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
@@ -521,6 +539,7 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
   if (rc) return rc;
   DtcParams p{};
   p.cu_k = a.cu_k;
+  p.batch = a.batch;
   p.q_len = a.q_len;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;

@@ -11,6 +11,9 @@ __global__ void __launch_bounds__(256)
     merge_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_md,
                  const float* __restrict__ sinks, int n_rows, int Hq, int S,
                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  // Launched as a programmatic dependent of the partial kernel: wait until
+  // that grid has completed and its writes are visible (immediate otherwise).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (w >= static_cast<long long>(n_rows) * Hq) return;
@@ -26,11 +29,24 @@ int launch_merge(const float* part_acc, const float* part_md, const float* sinks
   if (warps == 0) return SINKATTN_OK;
   const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
   auto* o = static_cast<__nv_bfloat16*>(out);
-  if (d == 64)
-    merge_kernel<64><<<blocks, 256, 0, stream>>>(part_acc, part_md, sinks, rows, Hq, num_splits, o, lse);
-  else
-    merge_kernel<128><<<blocks, 256, 0, stream>>>(part_acc, part_md, sinks, rows, Hq, num_splits, o, lse);
-  const cudaError_t e = cudaGetLastError();
+  // Programmatic stream serialisation: the launch may be processed while the
+  // previous kernel on the stream (the partial kernel) drains its last CTAs;
+  // the kernel's griddepcontrol.wait keeps the data dependency.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      d == 64 ? cudaLaunchKernelEx(&cfg, merge_kernel<64>, part_acc, part_md, sinks, rows, Hq,
+                                   num_splits, o, lse)
+              : cudaLaunchKernelEx(&cfg, merge_kernel<128>, part_acc, part_md, sinks, rows, Hq,
+                                   num_splits, o, lse);
   if (e != cudaSuccess) {
     set_error("merge kernel launch: %s", cudaGetErrorString(e));
     return SINKATTN_CUDA_ERROR;
