@@ -285,7 +285,7 @@ int sinkattn_merge(const float* part_acc, const float* part_md, const float* sin
     return fail(SINKATTN_UNSUPPORTED, "head_dim %d is not 64 or 128", head_dim);
   if (num_splits < 1) return fail(SINKATTN_INVALID_ARG, "num_splits must be at least 1");
   return launch_merge(part_acc, part_md, sinks, rows, num_qo_heads, head_dim, num_splits, out,
-                      lse, static_cast<cudaStream_t>(stream));
+                      lse, static_cast<cudaStream_t>(stream), false);
 }
 
 int sinkattn_decode_workspace_bytes(int32_t batch, int32_t q_len, int32_t num_qo_heads,
@@ -345,6 +345,8 @@ int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* 
   if (workspace_bytes < need)
     return fail(SINKATTN_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
   const size_t slots = static_cast<size_t>(batch) * q_len * num_qo_heads * num_splits;
   float* part_acc = static_cast<float*>(workspace);
   float* part_md = reinterpret_cast<float*>(static_cast<char*>(workspace) +
@@ -354,8 +356,9 @@ int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* 
                              part_acc, part_md, stream);
   if (rc) return rc;
   if (batch == 0) return SINKATTN_OK;
-  return sinkattn_merge(part_acc, part_md, sinks, batch * q_len, num_qo_heads, head_dim,
-                        num_splits, out, lse, stream);
+  // the partials are this call's scratch: the merge may drop them from L2
+  return launch_merge(part_acc, part_md, sinks, batch * q_len, num_qo_heads, head_dim,
+                      num_splits, out, lse, static_cast<cudaStream_t>(stream), true);
 }
 
 int sinkattn_decode_fused(const void* q, const void* k, const void* v, const int32_t* kv_indptr,

@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* stage = reinterpret_cast<float*>(smem + C::OFF_STG);
     const int S = p.num_splits;
+    const uint64_t keep_policy = policy_evict_last();
     for (int k = 0; k < n_mine; ++k) {
       const DtcItem t = item_of(k);
       if (!wwait(&o_full[k & 1], (k >> 1) & 1) || !wwait(&ml_full[k & 1], (k >> 1) & 1)) break;
@@ -508,7 +509,11 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
         const size_t rowid =
             static_cast<size_t>(t.q_start + t.q0 + t2) * p.Hq + t.kvh * G + (r - t2 * G);
         const float4 val = *reinterpret_cast<const float4*>(stage + r * C::XS + lane * 4);
-        *reinterpret_cast<float4*>(p.part_acc + (rowid * S + t.split) * D + lane * 4) = val;
+        // kept in L2 as long as possible: the merge reads the newest partials first
+        asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(
+                         p.part_acc + (rowid * S + t.split) * D + lane * 4),
+                     "f"(val.x), "f"(val.y), "f"(val.z), "f"(val.w), "l"(keep_policy)
+                     : "memory");
       }
       named_barrier_sync(1, 128);   // staging read before the next item overwrites it
     }

@@ -58,9 +58,12 @@ int launch_decode_tc(const AttnArgs& a, cudaStream_t stream);
 // Single-pass prefill on the tcgen05/TMEM path. Returns a SINKATTN_* status.
 int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
 
+// drop_partials: the partials are the library's scratch (sinkattn_decode's
+// workspace): after folding a row, drop its accumulator lines from L2 without
+// write-back. Never for caller-visible partials.
 int launch_merge(const float* part_acc, const float* part_md, const float* sinks, int32_t rows,
                  int32_t Hq, int32_t d, int32_t num_splits, void* out, float* lse,
-                 cudaStream_t stream);
+                 cudaStream_t stream, bool drop_partials);
 
 // Reads and clears the device status word of one translation unit.
 int read_status_attn_mma(cudaStream_t s, int* status);
