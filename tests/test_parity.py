@@ -205,12 +205,17 @@ def test_merge_accepts_rescaled_partials():
 
 
 TC_DECODE_CASES = [
-    # B, q_len, Hq, Hkv, G*QB rows, kv_range, S, window, q_scale
+    # B, q_len, Hq, Hkv, kv_range, S, window, q_scale   (rows per item = G x tokens)
     (3, 1, 64, 4, (1, 900), 2, 0, 3.0),        # 16 rows
-    (2, 4, 64, 8, (4, 1300), 1, 0, 3.0),       # GQA 8 x 4 tokens: 32 rows, 3 groups of tiles
-    (4, 3, 64, 4, (3, 2600), 2, 0, 4.0),       # 48 rows, peaky logits
+    (2, 4, 64, 8, (4, 1300), 1, 0, 3.0),       # GQA 8 x 4 tokens: 32 rows, one long chunk
+    (4, 3, 64, 4, (3, 2600), 2, 0, 4.0),       # 48 rows, peaky logits (lazy rescales)
     (2, 4, 32, 2, (4, 700), 3, 100, 1.0),      # 64 rows, window 100
-    (3, 7, 32, 2, (7, 400), 2, 0, 1.0),        # 64 rows: query blocks of 4 and 3 tokens
+    (3, 7, 32, 2, (7, 400), 2, 0, 1.0),        # 112 rows: one query block of 7 tokens
+    (2, 12, 32, 2, (12, 300), 3, 0, 1.0),      # 128-row tiles: query blocks of 8 and 4 tokens
+    (2, 3, 24, 2, (3, 500), 4, 0, 1.0),        # GQA 12: 36 real rows in a 48-row Q tile
+    (1, 2, 8, 8, (2, 200), 5, 9, 1.0),         # MHA (G 1), window 9, mostly empty chunks
+    (300, 3, 64, 4, (3, 64), 16, 0, 1.0),      # many short items per CTA, most chunks empty
+    (7, 3, 64, 4, (3000, 9000), 16, 0, 8.0),   # very peaky logits: rescales every few tiles
 ]
 
 
@@ -240,6 +245,26 @@ def test_tcgen05_decode_partials(case):
     want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
                                        inp["cu_k"], Hq, Hkv, d, scale, True, window)
     compare(out, lse, want_out, want_lse, "tcgen05 decode")
+
+
+def test_tcgen05_decode_without_staged_kv_indptr():
+    """More sequences than the kernel stages in shared memory (2048): every
+    role reads kv_indptr from global memory instead."""
+    B, q_len, Hq, Hkv, d, S = 2100, 1, 16, 1, 128, 2
+    inp = _decode_inputs(B, q_len, Hq, Hkv, d, (1, 40), seed=99)
+    scale = 1.0 / math.sqrt(d)
+    g = to_dev(inp)
+    max_kv = max(inp["kv_lens"])
+    sa.sinkattn_set_decode_kernel("tcgen05")
+    try:
+        out, lse = sa.sinkattn_decode(g["q"], g["k"], g["v"], g["cu_k"], g["sinks"], q_len, max_kv,
+                                      Hkv, num_splits=S, sm_scale=scale)
+        torch.cuda.synchronize()
+    finally:
+        sa.sinkattn_set_decode_kernel("auto")
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, True, 0)
+    compare(out, lse, want_out, want_lse, "tcgen05 decode, 2100 sequences")
 
 
 def test_tcgen05_decode_rejects_unsupported_shape():
