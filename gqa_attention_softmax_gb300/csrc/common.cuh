@@ -164,6 +164,14 @@ __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
   return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
 }
 
+// max(a, b, c) in one instruction (sm_100 family); like fmaxf, a NaN operand
+// is ignored.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x on the SFU (MUFU.EX2); exact 0 for -inf.
 __device__ __forceinline__ float ex2(float x) {
   float y;

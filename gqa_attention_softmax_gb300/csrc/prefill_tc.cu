@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], v[c][e]);
+        for (int e = 0; e < 32; e += 2)
+          mx4[(e >> 1) & 3] = fmax3(mx4[(e >> 1) & 3], v[c][e], v[c][e + 1]);
       // row maximum across the two halves
       my_x[0] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       mbar_arrive(&xch[t]);
