@@ -3,7 +3,9 @@
 Public API (thin wrappers over the C ABI in ``include/sinkattn.h``):
 ``sinkattn_prefill``, ``sinkattn_decode_split``, ``sinkattn_merge``,
 ``sinkattn_decode``, ``sinkattn_decode_fused``, ``sinkattn_decode_noalloc``, ``sinkattn_decode_workspace_bytes``,
-``sinkattn_decode_default_splits``, ``sinkattn_status_string``,
+``sinkattn_decode_default_splits``, ``sinkattn_prefill_paged``,
+``sinkattn_decode_split_paged``, ``sinkattn_decode_paged`` (paged KV cache),
+``sinkattn_status_string``,
 ``sinkattn_last_error``, ``sinkattn_debug_status``, ``sinkattn_set_decode_kernel``.
 
 The compiled library is loaded on first use; if it has not been built, every
@@ -17,11 +19,14 @@ from ._binding import (  # noqa: F401
     sinkattn_decode_default_splits,
     sinkattn_decode_fused,
     sinkattn_decode_noalloc,
+    sinkattn_decode_paged,
     sinkattn_decode_split,
+    sinkattn_decode_split_paged,
     sinkattn_decode_workspace_bytes,
     sinkattn_last_error,
     sinkattn_merge,
     sinkattn_prefill,
+    sinkattn_prefill_paged,
     sinkattn_set_decode_kernel,
     sinkattn_status_string,
 )

@@ -55,6 +55,12 @@ def lib() -> ctypes.CDLL:
                                                           ctypes.POINTER(SZ)]
             L.sinkattn_decode_default_splits.argtypes = [I32, I32, I32, I32, I32, I32,
                                                          ctypes.POINTER(I32)]
+            L.sinkattn_prefill_paged.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32,
+                                                 I32, I32, I32, I32, F, I32, I32, P, P, P]
+            L.sinkattn_decode_split_paged.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32,
+                                                      I32, I32, I32, F, I32, I32, I32, P, P, P]
+            L.sinkattn_decode_paged.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32,
+                                                I32, I32, F, I32, I32, I32, P, P, SZ, P, P, P]
             L.sinkattn_status_string.argtypes = [ctypes.c_int]
             L.sinkattn_status_string.restype = ctypes.c_char_p
             L.sinkattn_last_error.argtypes = []
@@ -64,7 +70,9 @@ def lib() -> ctypes.CDLL:
             for name in ("sinkattn_prefill", "sinkattn_decode_split", "sinkattn_merge",
                          "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc",
                          "sinkattn_decode_workspace_bytes", "sinkattn_decode_default_splits",
-                         "sinkattn_debug_status", "sinkattn_set_decode_kernel"):
+                         "sinkattn_debug_status", "sinkattn_set_decode_kernel",
+                         "sinkattn_prefill_paged", "sinkattn_decode_split_paged",
+                         "sinkattn_decode_paged"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -230,6 +238,82 @@ def sinkattn_decode_noalloc(q, k, v, kv_indptr, sinks, q_len, max_kv_len, num_kv
 
 
 DECODE_KERNELS = {"auto": 0, "warp": 1, "tcgen05": 2}
+
+
+def _pages(k_pages):
+    """(num_pages, Hkv, page_size, d) of a page pool."""
+    num_pages, Hkv, page_size, d = k_pages.shape
+    return num_pages, Hkv, page_size, d
+
+
+def sinkattn_prefill_paged(q, k_pages, v_pages, sinks, cu_seqlens_q, cu_seqlens_k, page_indptr,
+                           page_indices, max_seqlen_q, max_seqlen_k, sm_scale=None, causal=True,
+                           window=0, out=None, lse=None, return_lse=True, stream=None):
+    """sinkattn_prefill over a paged KV cache: k_pages, v_pages bf16
+    [num_pages, Hkv, page_size, d]; sequence b's pages are
+    page_indices[page_indptr[b]:page_indptr[b+1]] (int32, device); key
+    counts come from cu_seqlens_k. Returns (out, lse)."""
+    total_q, Hq, d = q.shape
+    num_pages, Hkv, page_size, _ = _pages(k_pages)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    rc = lib().sinkattn_prefill_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(sinks), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        _ptr(page_indptr), _ptr(page_indices), num_pages, page_size, cu_seqlens_q.numel() - 1,
+        total_q, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, d, _scale(sm_scale, d),
+        int(bool(causal)), int(window), _ptr(out), _ptr(lse), _stream(q, stream))
+    _check(rc)
+    return out, lse
+
+
+def sinkattn_decode_split_paged(q, k_pages, v_pages, kv_indptr, page_indptr, page_indices, q_len,
+                                max_kv_len, num_splits, sm_scale=None, causal=True, window=0,
+                                part_acc=None, part_md=None, stream=None):
+    """sinkattn_decode_split over a paged KV cache (layout as in
+    sinkattn_prefill_paged). Returns (part_acc, part_md) without the sink."""
+    rows, Hq, d = q.shape
+    num_pages, Hkv, page_size, _ = _pages(k_pages)
+    batch = kv_indptr.numel() - 1
+    if part_acc is None:
+        part_acc = torch.empty((rows, Hq, num_splits, d), dtype=torch.float32, device=q.device)
+    if part_md is None:
+        part_md = torch.empty((rows, Hq, num_splits, 2), dtype=torch.float32, device=q.device)
+    rc = lib().sinkattn_decode_split_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr), _ptr(page_indptr),
+        _ptr(page_indices), num_pages, page_size, batch, int(q_len), int(max_kv_len), Hq, Hkv, d,
+        _scale(sm_scale, d), int(bool(causal)), int(window), int(num_splits), _ptr(part_acc),
+        _ptr(part_md), _stream(q, stream))
+    _check(rc)
+    return part_acc, part_md
+
+
+def sinkattn_decode_paged(q, k_pages, v_pages, kv_indptr, page_indptr, page_indices, sinks, q_len,
+                          max_kv_len, num_splits=0, sm_scale=None, causal=True, window=0,
+                          workspace=None, out=None, lse=None, return_lse=True, stream=None):
+    """sinkattn_decode over a paged KV cache (layout as in
+    sinkattn_prefill_paged). Returns (out, lse)."""
+    rows, Hq, d = q.shape
+    num_pages, Hkv, page_size, _ = _pages(k_pages)
+    batch = kv_indptr.numel() - 1
+    if num_splits <= 0:
+        num_splits = sinkattn_decode_default_splits(batch, q_len, Hq, Hkv, d, max_kv_len)
+    need = sinkattn_decode_workspace_bytes(batch, q_len, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
+    rc = lib().sinkattn_decode_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr), _ptr(page_indptr),
+        _ptr(page_indices), num_pages, page_size, batch, int(q_len), int(max_kv_len), Hq, Hkv, d,
+        _scale(sm_scale, d), int(bool(causal)), int(window), int(num_splits), _ptr(sinks),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        _stream(q, stream))
+    _check(rc)
+    return out, lse
 
 
 def sinkattn_set_decode_kernel(kind) -> None:

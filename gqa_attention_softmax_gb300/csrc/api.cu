@@ -138,6 +138,33 @@ int check_common(const void* q, const void* k, const void* v, int32_t Hq, int32_
   return SINKATTN_OK;
 }
 
+// Paged KV: page pools [num_pages, Hkv, page_size, d] and per-sequence page lists.
+struct PagedKv {
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  int32_t num_pages;
+  int32_t page_size;
+};
+
+int check_paged(const PagedKv& pg, int32_t Hkv) {
+  if (!pg.page_indptr || !pg.page_indices)
+    return fail(SINKATTN_INVALID_ARG, "page_indptr and page_indices must be non-null");
+  if (pg.page_size < 16 || pg.page_size > 256 || (pg.page_size & (pg.page_size - 1)))
+    return fail(SINKATTN_UNSUPPORTED, "page_size %d is not a power of two in [16, 256]",
+                pg.page_size);
+  if (pg.num_pages < 1) return fail(SINKATTN_INVALID_ARG, "num_pages must be positive");
+  if (static_cast<int64_t>(pg.num_pages) * Hkv * pg.page_size >= (int64_t{1} << 31))
+    return fail(SINKATTN_UNSUPPORTED, "page pools exceed 2^31 rows");
+  return SINKATTN_OK;
+}
+
+void set_paged(AttnArgs* a, const PagedKv* pg) {
+  a->page_size = pg ? pg->page_size : 0;
+  a->num_pages = pg ? pg->num_pages : 0;
+  a->page_indptr = pg ? pg->page_indptr : nullptr;
+  a->page_indices = pg ? pg->page_indices : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -156,15 +183,19 @@ const char* sinkattn_status_string(int status) {
 
 const char* sinkattn_last_error(void) { return g_last_error; }
 
-int sinkattn_prefill(const void* q, const void* k, const void* v, const float* sinks,
-                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
-                     int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
-                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                     float sm_scale, int32_t causal, int32_t window, void* out, float* lse,
-                     void* stream) {
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(const void* q, const void* k, const void* v, const float* sinks,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const PagedKv* pg,
+                 int32_t batch, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                 int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, float sm_scale,
+                 int32_t causal, int32_t window, void* out, float* lse, void* stream) {
   g_last_error[0] = '\0';
   int rc = check_common(q, k, v, num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window);
   if (rc) return rc;
+  if (pg && (rc = check_paged(*pg, num_kv_heads))) return rc;
   if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
   if (!cu_seqlens_q || !cu_seqlens_k) return fail(SINKATTN_INVALID_ARG, "cu_seqlens must be non-null");
   if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
@@ -188,9 +219,39 @@ int sinkattn_prefill(const void* q, const void* k, const void* v, const float* s
   a.Hq = num_qo_heads; a.Hkv = num_kv_heads; a.d = head_dim;
   a.sm_scale = sm_scale; a.causal = causal; a.window = window; a.num_splits = 1;
   a.sinks = sinks; a.out = out; a.lse = lse;
+  set_paged(&a, pg);
   if (num_qo_heads / num_kv_heads > 128)
     return fail(SINKATTN_UNSUPPORTED, "GQA group of %d heads exceeds 128", num_qo_heads / num_kv_heads);
   return launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int sinkattn_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                     int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                     float sm_scale, int32_t causal, int32_t window, void* out, float* lse,
+                     void* stream) {
+  return prefill_impl(q, k, v, sinks, cu_seqlens_q, cu_seqlens_k, nullptr, batch, total_q,
+                      max_seqlen_q, max_seqlen_k, num_qo_heads, num_kv_heads, head_dim, sm_scale,
+                      causal, window, out, lse, stream);
+}
+
+int sinkattn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                           const float* sinks, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, const int32_t* page_indptr,
+                           const int32_t* page_indices, int32_t num_pages, int32_t page_size,
+                           int32_t batch, int32_t total_q, int32_t max_seqlen_q,
+                           int32_t max_seqlen_k, int32_t num_qo_heads, int32_t num_kv_heads,
+                           int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
+                           void* out, float* lse, void* stream) {
+  const PagedKv pg{page_indptr, page_indices, num_pages, page_size};
+  return prefill_impl(q, k_pages, v_pages, sinks, cu_seqlens_q, cu_seqlens_k, &pg, batch,
+                      total_q, max_seqlen_q, max_seqlen_k, num_qo_heads, num_kv_heads, head_dim,
+                      sm_scale, causal, window, out, lse, stream);
 }
 
 }  // extern "C"
@@ -240,6 +301,61 @@ int launch_partials(const AttnArgs& a, cudaStream_t stream) {
   return launch_attn_mma(a, stream);
 }
 
+int decode_split_impl(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
+                      const PagedKv* pg, int32_t batch, int32_t q_len, int32_t max_kv_len,
+                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                      float sm_scale, int32_t causal, int32_t window, int32_t num_splits,
+                      float* part_acc, float* part_md, void* stream) {
+  g_last_error[0] = '\0';
+  AttnArgs a;
+  int rc = decode_args(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads, num_kv_heads,
+                       head_dim, sm_scale, causal, window, num_splits, &a);
+  if (rc) return rc;
+  if (pg && (rc = check_paged(*pg, num_kv_heads))) return rc;
+  if (!part_acc || !part_md || !aligned16(part_acc) || !aligned16(part_md))
+    return fail(SINKATTN_INVALID_ARG, "partial buffers must be non-null and 16-byte aligned");
+  if (batch == 0) return SINKATTN_OK;
+  a.part_acc = part_acc; a.part_md = part_md;
+  set_paged(&a, pg);
+  return launch_partials(a, static_cast<cudaStream_t>(stream));
+}
+
+int decode_impl(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
+                const PagedKv* pg, int32_t batch, int32_t q_len, int32_t max_kv_len,
+                int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, float sm_scale,
+                int32_t causal, int32_t window, int32_t num_splits, const float* sinks,
+                void* workspace, size_t workspace_bytes, void* out, float* lse, void* stream) {
+  g_last_error[0] = '\0';
+  int rc;
+  if (num_splits <= 0) {
+    rc = sinkattn_decode_default_splits(batch, q_len, num_qo_heads, num_kv_heads, head_dim,
+                                        max_kv_len, &num_splits);
+    if (rc) return rc;
+  }
+  size_t need = 0;
+  rc = sinkattn_decode_workspace_bytes(batch, q_len, num_qo_heads, head_dim, num_splits, &need);
+  if (rc) return rc;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SINKATTN_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (workspace_bytes < need)
+    return fail(SINKATTN_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
+  const size_t slots = static_cast<size_t>(batch) * q_len * num_qo_heads * num_splits;
+  float* part_acc = static_cast<float*>(workspace);
+  float* part_md = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            ((slots * head_dim * 4 + 255) & ~static_cast<size_t>(255)));
+  rc = decode_split_impl(q, k, v, kv_indptr, pg, batch, q_len, max_kv_len, num_qo_heads,
+                         num_kv_heads, head_dim, sm_scale, causal, window, num_splits, part_acc,
+                         part_md, stream);
+  if (rc) return rc;
+  if (batch == 0) return SINKATTN_OK;
+  // the partials are this call's scratch: the merge may drop them from L2
+  return launch_merge(part_acc, part_md, sinks, batch * q_len, num_qo_heads, head_dim,
+                      num_splits, out, lse, static_cast<cudaStream_t>(stream), true);
+}
+
 }  // namespace
 
 extern "C" {
@@ -249,16 +365,22 @@ int sinkattn_decode_split(const void* q, const void* k, const void* v,
                           int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
                           int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
                           int32_t num_splits, float* part_acc, float* part_md, void* stream) {
-  g_last_error[0] = '\0';
-  AttnArgs a;
-  int rc = decode_args(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads, num_kv_heads,
-                       head_dim, sm_scale, causal, window, num_splits, &a);
-  if (rc) return rc;
-  if (!part_acc || !part_md || !aligned16(part_acc) || !aligned16(part_md))
-    return fail(SINKATTN_INVALID_ARG, "partial buffers must be non-null and 16-byte aligned");
-  if (batch == 0) return SINKATTN_OK;
-  a.part_acc = part_acc; a.part_md = part_md;
-  return launch_partials(a, static_cast<cudaStream_t>(stream));
+  return decode_split_impl(q, k, v, kv_indptr, nullptr, batch, q_len, max_kv_len, num_qo_heads,
+                           num_kv_heads, head_dim, sm_scale, causal, window, num_splits, part_acc,
+                           part_md, stream);
+}
+
+int sinkattn_decode_split_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* kv_indptr, const int32_t* page_indptr,
+                                const int32_t* page_indices, int32_t num_pages, int32_t page_size,
+                                int32_t batch, int32_t q_len, int32_t max_kv_len,
+                                int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                float sm_scale, int32_t causal, int32_t window, int32_t num_splits,
+                                float* part_acc, float* part_md, void* stream) {
+  const PagedKv pg{page_indptr, page_indices, num_pages, page_size};
+  return decode_split_impl(q, k_pages, v_pages, kv_indptr, &pg, batch, q_len, max_kv_len,
+                           num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window,
+                           num_splits, part_acc, part_md, stream);
 }
 
 int sinkattn_set_decode_kernel(int kind) {
@@ -330,35 +452,22 @@ int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* 
                     int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
                     int32_t window, int32_t num_splits, const float* sinks, void* workspace,
                     size_t workspace_bytes, void* out, float* lse, void* stream) {
-  g_last_error[0] = '\0';
-  int rc;
-  if (num_splits <= 0) {
-    rc = sinkattn_decode_default_splits(batch, q_len, num_qo_heads, num_kv_heads, head_dim,
-                                        max_kv_len, &num_splits);
-    if (rc) return rc;
-  }
-  size_t need = 0;
-  rc = sinkattn_decode_workspace_bytes(batch, q_len, num_qo_heads, head_dim, num_splits, &need);
-  if (rc) return rc;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return fail(SINKATTN_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
-  if (workspace_bytes < need)
-    return fail(SINKATTN_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
-  if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
-  const size_t slots = static_cast<size_t>(batch) * q_len * num_qo_heads * num_splits;
-  float* part_acc = static_cast<float*>(workspace);
-  float* part_md = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                            ((slots * head_dim * 4 + 255) & ~static_cast<size_t>(255)));
-  rc = sinkattn_decode_split(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads,
-                             num_kv_heads, head_dim, sm_scale, causal, window, num_splits,
-                             part_acc, part_md, stream);
-  if (rc) return rc;
-  if (batch == 0) return SINKATTN_OK;
-  // the partials are this call's scratch: the merge may drop them from L2
-  return launch_merge(part_acc, part_md, sinks, batch * q_len, num_qo_heads, head_dim,
-                      num_splits, out, lse, static_cast<cudaStream_t>(stream), true);
+  return decode_impl(q, k, v, kv_indptr, nullptr, batch, q_len, max_kv_len, num_qo_heads,
+                     num_kv_heads, head_dim, sm_scale, causal, window, num_splits, sinks,
+                     workspace, workspace_bytes, out, lse, stream);
+}
+
+int sinkattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* kv_indptr, const int32_t* page_indptr,
+                          const int32_t* page_indices, int32_t num_pages, int32_t page_size,
+                          int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
+                          int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
+                          int32_t window, int32_t num_splits, const float* sinks, void* workspace,
+                          size_t workspace_bytes, void* out, float* lse, void* stream) {
+  const PagedKv pg{page_indptr, page_indices, num_pages, page_size};
+  return decode_impl(q, k_pages, v_pages, kv_indptr, &pg, batch, q_len, max_kv_len, num_qo_heads,
+                     num_kv_heads, head_dim, sm_scale, causal, window, num_splits, sinks,
+                     workspace, workspace_bytes, out, lse, stream);
 }
 
 int sinkattn_decode_fused(const void* q, const void* k, const void* v, const int32_t* kv_indptr,

@@ -55,6 +55,10 @@ struct MmaParams {
   const float* sinks;     // fused mode
   __nv_bfloat16* out;     // fused mode
   float* lse;             // fused mode
+  // paged KV (page_size > 0): page-pool rows, boxes of box_rows keys
+  int page_size, box_rows;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
 };
 
 template <int D, int RT, int TG, int KT, int NST>
@@ -122,7 +126,12 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   int k_hi = min(k_lo + chunk, Lk);
   if (p.causal) k_hi = min(k_hi, posN + 1);
   if (p.window > 0) k_lo = max(k_lo, pos0 - p.window + 1);
-  const int ntiles = (k_hi > k_lo) ? (k_hi - k_lo + KT - 1) / KT : 0;
+  // Tiles end at k_hi (contiguous: no copy reads past the last key needed),
+  // or start on a multiple of KT (paged: no box straddles a page).
+  const bool paged = p.page_size > 0;
+  const int t0 = k_lo / KT * KT;
+  const int ntiles = (k_hi > k_lo) ? (k_hi - (paged ? t0 : k_lo) + KT - 1) / KT : 0;
+  const int first = paged ? t0 : k_hi - ntiles * KT;   // key of tile 0's first row
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -137,28 +146,60 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   // ------------------------------------------------------------------ producer
   bool writer = false;   // consumer warps holding the CTA's combined state
   if (warp == NW) {
-    if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    // The warp runs the loop (page lists are read 32 entries per warp load);
+    // lane 0 issues every copy.
+    if (ntiles > 0) {
+      const bool leader = (lane == 0);
+      if (leader) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
       const uint64_t policy = policy_evict_first();
-      const int slab = k_start * p.Hkv + kvh * Lk;   // tensor-map row of key 0
+      const int slab = k_start * p.Hkv + kvh * Lk;   // contiguous: tensor-map row of key 0
+      PageCursor pc;
+      if (paged) {
+        const int e0 = p.page_indptr[b];
+        const int np = p.page_indptr[b + 1] - e0;
+        if (leader && Lk > np * p.page_size) atomicExch(&g_status_attn_mma, SINKATTN_BAD_LENGTHS);
+        pc.start(p.page_indices + e0, np, first / p.page_size, lane);
+      }
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NST;
         const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
-        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
+          break;
         uint8_t* kt = tiles + st * C::STAGE_BYTES;
         uint8_t* vt = kt + C::TILE_BYTES;
-        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-        const int row = slab + k_hi - (ntiles - i) * KT;
+        if (leader) mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+        const int j0 = first + i * KT;
+        if (!paged) {
+          if (leader) {
 #pragma unroll
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          tma_load_2d_hint(kt + sub * C::SUB_BYTES, &tmK, sub * 64, row, &full[st], policy);
-          tma_load_2d_hint(vt + sub * C::SUB_BYTES, &tmV, sub * 64, row, &full[st], policy);
+            for (int sub = 0; sub < C::NSUB; ++sub) {
+              tma_load_2d_hint(kt + sub * C::SUB_BYTES, &tmK, sub * 64, slab + j0, &full[st], policy);
+              tma_load_2d_hint(vt + sub * C::SUB_BYTES, &tmV, sub * 64, slab + j0, &full[st], policy);
+            }
+          }
+        } else {
+          // one box per page segment, lane i issuing box i: rows (page,
+          // head, slot) of the pool
+          const int nbox = KT / p.box_rows;
+          const int a = j0 + min(lane, nbox - 1) * p.box_rows;
+          const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
+          if (lane < nbox) {
+            const int row = (page * p.Hkv + kvh) * p.page_size + a % p.page_size;
+            const int off = (a - j0) * 128;
+#pragma unroll
+            for (int sub = 0; sub < C::NSUB; ++sub) {
+              tma_load_2d_hint(kt + sub * C::SUB_BYTES + off, &tmK, sub * 64, row, &full[st], policy);
+              tma_load_2d_hint(vt + sub * C::SUB_BYTES + off, &tmV, sub * 64, row, &full[st], policy);
+            }
+          }
         }
         issued = i + 1;
       }
-      if (*abort_flag) {   // let every copy land before the CTA's shared memory goes away
+      if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
         for (int i = max(0, issued - NST); i < issued; ++i)
           mbar_drain(&full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
       }
@@ -214,7 +255,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
     if (!mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma)) break;
     const uint32_t kbase = smem_u32(tiles + st * C::STAGE_BYTES);
     const uint32_t vbase = kbase + C::TILE_BYTES;
-    const int j0 = k_hi - (ntiles - i) * KT;   // key index of tile row 0
+    const int j0 = first + i * KT;   // key index of tile row 0
 
     float s[KT / 8][4];
 #pragma unroll
@@ -235,7 +276,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
     }
 
     // Mask (skipped for tiles that every row sees whole).
-    const bool whole = (j0 >= k_lo) && (!p.causal || j0 + KT - 1 <= pos0) &&
+    const bool whole = (j0 >= k_lo) && (j0 + KT <= k_hi) && (!p.causal || j0 + KT - 1 <= pos0) &&
                        (p.window <= 0 || j0 > posN - p.window);
     if (!whole) {
 #pragma unroll
@@ -244,7 +285,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
         for (int e = 0; e < 4; ++e) {
           const int key = j0 + 8 * j + (lane & 3) * 2 + (e & 1);
           const int ps = pos[e >> 1];
-          const bool vis = key >= k_lo && (!p.causal || key <= ps) &&
+          const bool vis = key >= k_lo && key < k_hi && (!p.causal || key <= ps) &&
                            (p.window <= 0 || key > ps - p.window);
           if (!vis) s[j][e] = NEG_INF;
         }
@@ -472,10 +513,11 @@ template <int D, int RT, int TG, int KT, int NST, bool FUSED>
 static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   using C = MmaCfg<D, RT, TG, KT, NST>;
   CUtensorMap tmK, tmV;
-  const uint64_t rows = static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
-  int rc = make_rows_tmap(&tmK, a.k, rows, D, KT, 128);
+  const uint64_t rows = kv_map_rows(a);
+  const int box = kv_box_rows(a, KT);
+  int rc = make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
-  rc = make_rows_tmap(&tmV, a.v, rows, D, KT, 128);
+  rc = make_rows_tmap(&tmV, a.v, rows, D, box, 128);
   if (rc) return rc;
 
   MmaParams p{};
@@ -497,6 +539,10 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   p.window = a.window;
   p.part_acc = a.part_acc;
   p.part_md = a.part_md;
+  p.page_size = a.page_size;
+  p.box_rows = box;
+  p.page_indptr = a.page_indptr;
+  p.page_indices = a.page_indices;
   p.sinks = a.sinks;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;

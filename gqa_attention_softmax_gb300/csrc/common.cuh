@@ -164,6 +164,43 @@ __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
   return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
 }
 
+// ---------------------------------------------------------------------------
+// Paged KV: a producer warp's view of one sequence's page list.
+// Entry e of the list (global memory) is the page holding keys
+// [e * page_size, (e + 1) * page_size). Lane l caches entry base + l and the
+// entry 32 further, so a warp reads the list 32 entries per load, one batch
+// ahead of use; entries past the end repeat the last page (its keys are
+// masked wherever they fall outside the sequence); an empty list reads page 0
+// (the caller records the length error). get() is warp-collective: it moves
+// the cursor to entry `e_first` (non-decreasing across calls) and returns to
+// each lane the page of its own entry `e`, which must lie in the same aligned
+// group of 32 entries as e_first -- true for the entries of one KV tile, whose
+// KT / page_size pages (a power of two up to 8) start on a multiple of that
+// count.
+// ---------------------------------------------------------------------------
+struct PageCursor {
+  const int32_t* list;
+  int count, base, cur, nxt;
+  __device__ __forceinline__ int load(int e) const {
+    return count > 0 ? list[e < count ? e : count - 1] : 0;
+  }
+  __device__ __forceinline__ void start(const int32_t* list_, int count_, int e0, int lane) {
+    list = list_;
+    count = count_;
+    base = e0 & ~31;
+    cur = load(base + lane);
+    nxt = load(base + 32 + lane);
+  }
+  __device__ __forceinline__ int get(int e_first, int e, int lane) {
+    while (e_first >= base + 32) {
+      base += 32;
+      cur = nxt;
+      nxt = load(base + 32 + lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, e - base);
+  }
+};
+
 // max(a, b, c) in one instruction (sm_100 family); like fmaxf, a NaN operand
 // is ignored.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

@@ -53,11 +53,17 @@ struct DtcParams {
   int causal, window;
   float* part_acc;
   float* part_md;
+  // paged KV (page_size > 0): page-pool rows, boxes of box_rows keys
+  int page_size, box_rows;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
 };
 
 // One work item: (sequence b, KV head, query block, KV chunk) and its keys.
 struct DtcItem {
   int b, kvh, split, q_start, q0, nq, k_start, Lk, pos0, k_lo, k_hi, n;
+  int first;   // key of tile 0's first column: tiles end at k_hi (contiguous) or
+               // start on a multiple of the tile (paged, so boxes never straddle pages)
 };
 
 // cu_k is read from `cu` (a shared-memory copy when the batch fits, else
@@ -84,7 +90,14 @@ __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* c
   t.k_hi = min(t.k_lo + chunk, t.Lk);
   if (p.causal) t.k_hi = min(t.k_hi, posN + 1);
   if (p.window > 0) t.k_lo = max(t.k_lo, t.pos0 - p.window + 1);
-  t.n = (t.k_hi > t.k_lo) ? (t.k_hi - t.k_lo + KT - 1) / KT : 0;
+  if (p.page_size > 0) {
+    const int t0 = t.k_lo / KT * KT;
+    t.n = (t.k_hi > t.k_lo) ? (t.k_hi - t0 + KT - 1) / KT : 0;
+    t.first = t0;
+  } else {
+    t.n = (t.k_hi > t.k_lo) ? (t.k_hi - t.k_lo + KT - 1) / KT : 0;
+    t.first = t.k_hi - t.n * KT;
+  }
   return t;
 }
 
@@ -221,43 +234,76 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
 
   if (warp == 10) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
+    // The warp runs the loop (page lists are read 32 entries per warp load);
+    // lane 0 issues every copy.
+    const bool leader = (lane == 0);
+    if (leader) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const uint64_t policy = policy_evict_first();   // K/V are streamed once
-      int g = 0, qi = 0;                               // tile and non-empty item ordinals
-      bool ok = true;
-      for (int k = 0; ok && k < n_mine; ++k) {
-        const DtcItem t = item_of(k);
-        if (t.Lk < p.q_len || t.Lk > p.max_kv) atomicExch(status, SINKATTN_BAD_LENGTHS);
-        if (t.n == 0) continue;
-        ok = mbar_wait(&q_empty[qi & 1], ((qi >> 1) & 1) ^ 1, abort_flag, status);
-        if (!ok) break;
+    }
+    const uint64_t policy = policy_evict_first();   // K/V are streamed once
+    const bool paged = p.page_size > 0;
+    PageCursor pc;
+    int g = 0, qi = 0;                               // tile and non-empty item ordinals
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const DtcItem t = item_of(k);
+      if (leader && (t.Lk < p.q_len || t.Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
+      if (t.n == 0) continue;
+      if (!wwait(&q_empty[qi & 1], ((qi >> 1) & 1) ^ 1)) { ok = false; break; }
+      if (leader) {
         mbar_arrive_expect_tx(&q_full[qi & 1], static_cast<uint32_t>(2 * 128 * p.G * p.QB));
         for (int sub = 0; sub < 2; ++sub)
           tc::tma_load_3d(smem + C::OFF_Q + (qi & 1) * C::Q_BUF + sub * C::Q_SUB, &tmQ, sub * 64,
                           t.kvh * p.G, t.q_start + t.q0, &q_full[qi & 1]);
-        ++qi;
-        const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // tensor-map row of key 0
-        for (int j = 0; j < t.n; ++j, ++g) {
-          const int st = g % NST;
-          if (!mbar_wait(&kv_empty[st], ((g / NST) & 1) ^ 1, abort_flag, status)) { ok = false; break; }
-          uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
-          mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-          const int row = slab + t.k_hi - (t.n - j) * KT;
+      }
+      ++qi;
+      if (paged) {
+        const int e0 = p.page_indptr[t.b];
+        const int np = p.page_indptr[t.b + 1] - e0;
+        if (leader && t.Lk > np * p.page_size) atomicExch(status, SINKATTN_BAD_LENGTHS);
+        pc.start(p.page_indices + e0, np, t.first / p.page_size, lane);
+      }
+      const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // contiguous: tensor-map row of key 0
+      for (int j = 0; j < t.n; ++j, ++g) {
+        const int st = g % NST;
+        if (!wwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
+        uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
+        if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+        const int j0 = t.first + j * KT;
+        if (!paged) {
+          if (leader) {
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            tma_load_2d_hint(kt + sub * C::SUB_KV, &tmK, sub * 64, row, &kv_full[st], policy);
-            tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV, &tmV, sub * 64, row, &kv_full[st],
-                             policy);
+            for (int sub = 0; sub < 2; ++sub) {
+              tma_load_2d_hint(kt + sub * C::SUB_KV, &tmK, sub * 64, slab + j0, &kv_full[st], policy);
+              tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV, &tmV, sub * 64, slab + j0,
+                               &kv_full[st], policy);
+            }
+          }
+        } else {
+          // one box per page segment, lane i issuing box i: rows (page,
+          // head, slot) of the pool
+          const int nbox = KT / p.box_rows;
+          const int a = j0 + min(lane, nbox - 1) * p.box_rows;
+          const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
+          if (lane < nbox) {
+            const int row = (page * p.Hkv + t.kvh) * p.page_size + a % p.page_size;
+            const int off = (a - j0) * 128;
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+              tma_load_2d_hint(kt + sub * C::SUB_KV + off, &tmK, sub * 64, row, &kv_full[st],
+                               policy);
+              tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV + off, &tmV, sub * 64, row,
+                               &kv_full[st], policy);
+            }
           }
         }
       }
-      if (*abort_flag) {   // let every copy land before the CTA's shared memory goes away
-        for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
-        for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
-      }
+    }
+    if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
+      for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
+      for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
     }
   } else if (warp == 11) {
     // ---------------------------------------------------------------- MMA issuer
@@ -382,7 +428,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
         }
         tc::fence_after_sync();
         const uint32_t s_addr = lane_base + static_cast<uint32_t>((g & 3) * KT);
-        const int j0 = t.k_hi - (t.n - j) * KT;   // key of tile column 0
+        const int j0 = t.first + j * KT;   // key of tile column 0
         float v[2][32];
         tc::tmem_ld32(s_addr, v[0]);
         tc::tmem_ld32(s_addr + 32, v[1]);
@@ -538,12 +584,17 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
   CUtensorMap tmQ, tmK, tmV;
   int rc = make_q_tmap(&tmQ, a.q, static_cast<uint64_t>(a.batch) * a.q_len, a.Hq, C::D, G, QB);
   if (rc) return rc;
-  const uint64_t rows = static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
-  rc = make_rows_tmap(&tmK, a.k, rows, C::D, C::KT, 128);
+  const uint64_t rows = kv_map_rows(a);
+  const int box = kv_box_rows(a, C::KT);
+  rc = make_rows_tmap(&tmK, a.k, rows, C::D, box, 128);
   if (rc) return rc;
-  rc = make_rows_tmap(&tmV, a.v, rows, C::D, C::KT, 128);
+  rc = make_rows_tmap(&tmV, a.v, rows, C::D, box, 128);
   if (rc) return rc;
   DtcParams p{};
+  p.page_size = a.page_size;
+  p.box_rows = box;
+  p.page_indptr = a.page_indptr;
+  p.page_indices = a.page_indices;
   p.cu_k = a.cu_k;
   p.batch = a.batch;
   p.q_len = a.q_len;

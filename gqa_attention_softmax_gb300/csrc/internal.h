@@ -28,7 +28,24 @@ struct AttnArgs {
   // split mode
   float* part_acc;
   float* part_md;
+  // paged KV (page_size > 0): k and v are page pools [num_pages, Hkv, page_size, d];
+  // sequence b's keys [e * page_size, (e + 1) * page_size) live in page
+  // page_indices[page_indptr[b] + e]; cu_k still gives the key counts
+  int32_t page_size;
+  int32_t num_pages;
+  const int32_t* page_indptr;   // [B+1]
+  const int32_t* page_indices;  // [page_indptr[B]]
 };
+
+// Rows of the 2-D tensor map over K or V, and the box height: contiguous HND
+// rows, or page-pool rows (page, head, slot) with boxes of min(page, tile) rows.
+inline uint64_t kv_map_rows(const AttnArgs& a) {
+  return a.page_size > 0 ? static_cast<uint64_t>(a.num_pages) * a.Hkv * a.page_size
+                         : static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
+}
+inline int kv_box_rows(const AttnArgs& a, int tile_keys) {
+  return (a.page_size > 0 && a.page_size < tile_keys) ? a.page_size : tile_keys;
+}
 
 // Encodes a 2-D tensor map over a [rows, d] bf16 buffer with [box_rows, 64]
 // boxes and 128-byte swizzling. Returns 0 or a SINKATTN_* status.

@@ -56,6 +56,10 @@ struct TcParams {
   const float* sinks;
   __nv_bfloat16* out;
   float* lse;
+  // paged KV (page_size > 0): page-pool rows, boxes of box_rows keys
+  int page_size, box_rows;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
 };
 
 template <int D, int NST>
@@ -128,7 +132,12 @@ __global__ void __launch_bounds__(576, 1)
   int k_lo = 0, k_hi = Lk;
   if (p.causal) k_hi = min(k_hi, posN + 1);
   if (p.window > 0) k_lo = max(k_lo, pos0 - p.window + 1);
-  const int n = (k_hi > k_lo) ? (k_hi - k_lo + KT - 1) / KT : 0;
+  // Tiles end at k_hi (contiguous: no copy reads past the last key needed),
+  // or start on a multiple of KT (paged: no box straddles a page).
+  const bool paged = p.page_size > 0;
+  const int t0 = k_lo / KT * KT;
+  const int n = (k_hi > k_lo) ? (k_hi - (paged ? t0 : k_lo) + KT - 1) / KT : 0;
+  const int first = paged ? t0 : k_hi - n * KT;   // key of tile 0's first column
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -163,7 +172,10 @@ __global__ void __launch_bounds__(576, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
+    // The warp runs the loop (page lists are read 32 entries per warp load);
+    // lane 0 issues every copy.
+    const bool leader = (lane == 0);
+    if (leader) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -175,28 +187,56 @@ __global__ void __launch_bounds__(576, 1)
         for (int sub = 0; sub < C::NSUB; ++sub)
           tc::tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + sub * C::SUB, &tmQ, sub * 64,
                           kvh * p.G, q_start + q0 + t * p.QB, q_full);
-      const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
-      const int slab = k_start * p.Hkv + kvh * Lk;
-      int issued = 0;
-      for (int i = 0; i < n; ++i) {
-        const int st = i % NST;
-        if (!mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1, abort_flag, status)) break;
-        uint8_t* kt = smem + C::OFF_KV + st * C::STAGE;
-        mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-        const int row = slab + k_hi - (n - i) * KT;
+    }
+    const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
+    const int slab = k_start * p.Hkv + kvh * Lk;     // contiguous: tensor-map row of key 0
+    PageCursor pc;
+    if (paged && n > 0) {
+      const int e0 = p.page_indptr[b];
+      const int np = p.page_indptr[b + 1] - e0;
+      if (leader && Lk > np * p.page_size) atomicExch(status, SINKATTN_BAD_LENGTHS);
+      pc.start(p.page_indices + e0, np, first / p.page_size, lane);
+    }
+    int issued = 0;
+    for (int i = 0; i < n; ++i) {
+      const int st = i % NST;
+      if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1, abort_flag, status)))
+        break;
+      uint8_t* kt = smem + C::OFF_KV + st * C::STAGE;
+      if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+      const int j0 = first + i * KT;
+      if (!paged) {
+        if (leader) {
 #pragma unroll
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          tma_load_2d_hint(kt + sub * C::SUB, &tmK, sub * 64, row, &kv_full[st], policy);
-          tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB, &tmV, sub * 64, row, &kv_full[st],
-                           policy);
+          for (int sub = 0; sub < C::NSUB; ++sub) {
+            tma_load_2d_hint(kt + sub * C::SUB, &tmK, sub * 64, slab + j0, &kv_full[st], policy);
+            tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB, &tmV, sub * 64, slab + j0,
+                             &kv_full[st], policy);
+          }
         }
-        issued = i + 1;
+      } else {
+        // one box per page segment, lane i issuing box i: rows (page, head,
+        // slot) of the pool
+        const int nbox = KT / p.box_rows;
+        const int a = j0 + min(lane, nbox - 1) * p.box_rows;
+        const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
+        if (lane < nbox) {
+          const int row = (page * p.Hkv + kvh) * p.page_size + a % p.page_size;
+          const int off = (a - j0) * 128;
+#pragma unroll
+          for (int sub = 0; sub < C::NSUB; ++sub) {
+            tma_load_2d_hint(kt + sub * C::SUB + off, &tmK, sub * 64, row, &kv_full[st], policy);
+            tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB + off, &tmV, sub * 64, row,
+                             &kv_full[st], policy);
+          }
+        }
       }
-      if (*abort_flag) {
-        mbar_drain(q_full, 0);
-        for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_drain(&kv_full[i % NST], (i / NST) & 1);
-      }
+      issued = i + 1;
+    }
+    if (leader && *abort_flag) {
+      mbar_drain(q_full, 0);
+      for (int i = max(0, issued - NST); i < issued; ++i)
+        mbar_drain(&kv_full[i % NST], (i / NST) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -333,7 +373,7 @@ __global__ void __launch_bounds__(576, 1)
     for (int j = 0; j < n; ++j) {
       if (!wwait(&s_full[t], j & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      const int j0 = k_hi - (n - j) * KT;
+      const int j0 = first + j * KT;
       const bool masked = (j0 < lo_r || j0 + KT - 1 > hi_r);
       const int clo = lo_r - j0 - 64 * hf, chi = hi_r - j0 - 64 * hf;
 
@@ -492,13 +532,18 @@ static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
   const int QB = 128 / G;
   int rc = make_q_tmap(&tmQ, a.q, static_cast<uint64_t>(a.total_q), a.Hq, D, G, QB);
   if (rc) return rc;
-  const uint64_t rows = static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
-  rc = make_rows_tmap(&tmK, a.k, rows, D, C::KT, 128);
+  const uint64_t rows = kv_map_rows(a);
+  const int box = kv_box_rows(a, C::KT);
+  rc = make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
-  rc = make_rows_tmap(&tmV, a.v, rows, D, C::KT, 128);
+  rc = make_rows_tmap(&tmV, a.v, rows, D, box, 128);
   if (rc) return rc;
 
   TcParams p{};
+  p.page_size = a.page_size;
+  p.box_rows = box;
+  p.page_indptr = a.page_indptr;
+  p.page_indices = a.page_indices;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
   p.Hq = a.Hq;

@@ -13,6 +13,10 @@ Layouts (heads-leading KV cache, "Hosting Qwen on Blackwell", section
 * ``k``, ``v``: bf16 ragged HND ``[Hkv * total_k, d]``: sequence ``b`` is the
   contiguous block ``[Hkv, Lk_b, d]`` starting at row ``Hkv * cu_k[b]``.
 * ``sinks``: fp32 ``[Hq]``; ``cu_q``, ``cu_k``: int32 ``[B + 1]``.
+* paged KV (``to_paged``): pools ``k_pages``, ``v_pages`` bf16
+  ``[num_pages, Hkv, page_size, d]``; sequence ``b``'s keys
+  ``[e * page_size, (e + 1) * page_size)`` sit in page
+  ``page_indices[page_indptr[b] + e]``.
 
 Draw order (fixed, so a seed names one input set): key lengths, then Q, K, V,
 sinks. Q/K/V are drawn as fp32 normals then rounded to bf16 (round to nearest
@@ -153,3 +157,43 @@ def explicit_inputs(q_lens, kv_lens, Hq, Hkv, d, seed=0, device="cpu",
                  q_lens=list(q_lens), sink_dist=sink_dist, seed=seed)
     return make_inputs(w, device=device, q_scale=q_scale)
 
+
+
+def to_paged(inp: dict, Hkv: int, page_size: int, seed: int = 0, spare_pages: int = 3,
+             fill_scale: float = 100.0, shuffle: bool = True) -> dict:
+    """Scatter the ragged HND ``k``/``v`` of ``inp`` into page pools.
+
+    Pages are handed out in a seeded random order (in pool order if not
+    ``shuffle``), plus ``spare_pages`` that no sequence uses; every slot that holds no key of a sequence -- the tail of
+    each sequence's last page and the spare pages -- is filled with large
+    finite values (N(0, fill_scale^2), bf16), so a kernel that lets such a slot
+    through its mask shows it. Returns k_pages, v_pages, page_indptr,
+    page_indices on the device of ``inp["k"]``. Pure data movement.
+    """
+    k, v = inp["k"], inp["v"]
+    dev = k.device
+    d = k.shape[1]
+    kv_lens = list(inp["kv_lens"])
+    n_b = [(L + page_size - 1) // page_size for L in kv_lens]
+    used = sum(n_b)
+    total = used + spare_pages
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    perm = torch.randperm(total, generator=gen) if shuffle else torch.arange(total)
+    shape = (total, Hkv, page_size, d)
+    kp = (torch.randn(shape, generator=gen) * fill_scale).to(torch.bfloat16)
+    vp = (torch.randn(shape, generator=gen) * fill_scale).to(torch.bfloat16)
+    k_cpu, v_cpu = k.cpu(), v.cpu()
+    indptr = [0]
+    r0 = 0
+    for L, n in zip(kv_lens, n_b):
+        idx = perm[indptr[-1]:indptr[-1] + n]
+        for src, pool in ((k_cpu, kp), (v_cpu, vp)):
+            blk = src[r0:r0 + Hkv * L].view(Hkv, L, d)
+            cur = pool[idx].permute(1, 0, 2, 3).reshape(Hkv, n * page_size, d)
+            cur[:, :L] = blk
+            pool[idx] = cur.view(Hkv, n, page_size, d).permute(1, 0, 2, 3)
+        indptr.append(indptr[-1] + n)
+        r0 += Hkv * L
+    return dict(k_pages=kp.to(dev), v_pages=vp.to(dev),
+                page_indptr=torch.tensor(indptr, dtype=torch.int32, device=dev),
+                page_indices=perm[:used].to(torch.int32).to(dev))

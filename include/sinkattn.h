@@ -229,6 +229,57 @@ SINKATTN_API int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, in
 #define SINKATTN_DECODE_TCGEN05 2
 SINKATTN_API int sinkattn_set_decode_kernel(int kind);
 
+/*
+ * Paged KV cache (HND within a page: heads leading, tokens contiguous): the
+ * same operations as sinkattn_prefill, sinkattn_decode_split and
+ * sinkattn_decode, with K and V held in page pools
+ *   k_pages, v_pages: bf16 [num_pages, Hkv, page_size, d] (device)
+ * and sequence b's keys [e * page_size, (e + 1) * page_size) in page
+ * page_indices[page_indptr[b] + e]:
+ *   page_indptr  int32 [batch + 1] (device), page_indices int32
+ *   [page_indptr[batch]] (device), each entry in [0, num_pages).
+ * Key counts still come from cu_seqlens_k / kv_indptr (only their
+ * differences are used); sequence b needs at least ceil(Lk_b / page_size)
+ * pages -- fewer makes the kernel record SINKATTN_BAD_LENGTHS (see
+ * sinkattn_debug_status). page_size is a power of two in [16, 256]
+ * (SINKATTN_UNSUPPORTED otherwise); num_pages * Hkv * page_size < 2^31.
+ * Slots of the last page past Lk_b are read and masked (weight 0): they must
+ * hold finite values (a zero-initialised pool does). A page index outside
+ * [0, num_pages) gives undefined values for its sequence but no read outside
+ * the pools (the copy engine bounds every copy by the pool's extent).
+ * Every other argument, layout, rule and result is that of the contiguous
+ * entry point; in particular the partials and the merge are the same.
+ */
+SINKATTN_API int sinkattn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                                        const float* sinks, const int32_t* cu_seqlens_q,
+                                        const int32_t* cu_seqlens_k, const int32_t* page_indptr,
+                                        const int32_t* page_indices, int32_t num_pages,
+                                        int32_t page_size, int32_t batch, int32_t total_q,
+                                        int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                        int32_t num_qo_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, float sm_scale, int32_t causal,
+                                        int32_t window, void* out, float* lse, void* stream);
+SINKATTN_API int sinkattn_decode_split_paged(const void* q, const void* k_pages,
+                                             const void* v_pages, const int32_t* kv_indptr,
+                                             const int32_t* page_indptr,
+                                             const int32_t* page_indices, int32_t num_pages,
+                                             int32_t page_size, int32_t batch, int32_t q_len,
+                                             int32_t max_kv_len, int32_t num_qo_heads,
+                                             int32_t num_kv_heads, int32_t head_dim,
+                                             float sm_scale, int32_t causal, int32_t window,
+                                             int32_t num_splits, float* part_acc, float* part_md,
+                                             void* stream);
+SINKATTN_API int sinkattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* kv_indptr, const int32_t* page_indptr,
+                                       const int32_t* page_indices, int32_t num_pages,
+                                       int32_t page_size, int32_t batch, int32_t q_len,
+                                       int32_t max_kv_len, int32_t num_qo_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, float sm_scale,
+                                       int32_t causal, int32_t window, int32_t num_splits,
+                                       const float* sinks, void* workspace,
+                                       size_t workspace_bytes, void* out, float* lse,
+                                       void* stream);
+
 /* Human-readable name of a status code (static string). */
 SINKATTN_API const char* sinkattn_status_string(int status);
 

@@ -145,3 +145,60 @@ def test_default_splits_bounds(L):
     s = sa.sinkattn_decode_default_splits(64, 1, 64, 8, 64, 8192)
     assert 1 <= s <= 64
     assert sa.sinkattn_decode_default_splits(1, 1, 8, 1, 64, 100) == 1   # short: no split
+
+
+def prefill_paged(L, **kw):
+    args = dict(q=A, k=B, v=C, sinks=None, cuq=0x5000, cuk=0x6000, pind=0x9000, pidx=0xA000,
+                npages=8, psize=64, batch=1, total_q=16, maxq=16, maxk=128, hq=4, hkv=1, d=64,
+                scale=0.125, causal=1, window=0, out=O, lse=None)
+    args.update(kw)
+    return L.sinkattn_prefill_paged(
+        args["q"], args["k"], args["v"], args["sinks"], args["cuq"], args["cuk"], args["pind"],
+        args["pidx"], args["npages"], args["psize"], args["batch"], args["total_q"], args["maxq"],
+        args["maxk"], args["hq"], args["hkv"], args["d"], args["scale"], args["causal"],
+        args["window"], args["out"], args["lse"], None)
+
+
+def split_paged(L, **kw):
+    args = dict(q=A, k=B, v=C, ind=0x5000, pind=0x9000, pidx=0xA000, npages=8, psize=64, batch=2,
+                qlen=1, maxk=100, hq=8, hkv=1, d=128, scale=0.1, causal=1, window=0, S=4,
+                acc=0x7000, md=0x8000)
+    args.update(kw)
+    return L.sinkattn_decode_split_paged(
+        args["q"], args["k"], args["v"], args["ind"], args["pind"], args["pidx"], args["npages"],
+        args["psize"], args["batch"], args["qlen"], args["maxk"], args["hq"], args["hkv"],
+        args["d"], args["scale"], args["causal"], args["window"], args["S"], args["acc"],
+        args["md"], None)
+
+
+PAGED_BAD = [
+    (dict(pind=None), 1),
+    (dict(pidx=None), 1),
+    (dict(psize=8), 2),              # below 16
+    (dict(psize=48), 2),             # not a power of two
+    (dict(psize=512), 2),            # above 256
+    (dict(npages=0), 1),
+    (dict(npages=1 << 24, psize=256), 2),   # pool rows reach 2^31
+    (dict(k=B + 8), 1),              # misaligned pool
+]
+
+
+@pytest.mark.parametrize("kw,status", PAGED_BAD)
+def test_prefill_paged_rejects_bad_arguments(L, kw, status):
+    assert prefill_paged(L, **kw) == status
+    assert sa.sinkattn_last_error() != ""
+
+
+@pytest.mark.parametrize("kw,status", PAGED_BAD + [(dict(S=0), 1), (dict(d=32), 2)])
+def test_decode_split_paged_rejects_bad_arguments(L, kw, status):
+    assert split_paged(L, **kw) == status
+
+
+def test_decode_paged_checks_workspace_before_launch(L):
+    need = sa.sinkattn_decode_workspace_bytes(2, 1, 8, 128, 4)
+    rc = L.sinkattn_decode_paged(A, B, C, 0x5000, 0x9000, 0xA000, 8, 64, 2, 1, 100, 8, 1, 128, 0.1,
+                                 1, 0, 4, None, 0x10000, need - 1, O, None, None)
+    assert rc == 1 and "workspace" in sa.sinkattn_last_error()
+    rc = L.sinkattn_decode_paged(A, B, C, 0x5000, 0x9000, 0xA000, 8, 16, 2, 1, 100, 8, 1, 128, 0.1,
+                                 1, 0, 4, None, 0x10000, need, O, None, None)
+    assert rc != 1 or "workspace" not in sa.sinkattn_last_error()
