@@ -32,7 +32,8 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 HEADLINE = "gptoss_decode"
-ALSO = ["qwen_mtp_decode", "gptoss_prefill", "gptoss_prefill_w128", "qwen_prefill"]
+ALSO = ["qwen_mtp_decode", "gptoss_prefill", "gptoss_prefill_w128", "qwen_prefill",
+        "gptoss_decode_paged", "qwen_mtp_decode_paged"]
 METRIC = "decode KV-read HBM GB/s and prefill TFLOP/s, each as % of GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2**20
@@ -69,6 +70,8 @@ def work(w, inp):
         kv_tok = sum(inp["kv_lens"])
     kv_bytes = 2 * Hkv * kv_tok * d * 2
     small = Hq * 4 + (inp["batch"] + 1) * 4 * (1 if w.kind == "decode" else 2)
+    if w.page_size > 0:   # page lists
+        small += 4 * (inp["batch"] + 1 + sum(-(-lk // w.page_size) for lk in inp["kv_lens"]))
     total = q_bytes + kv_bytes + q_bytes + tq * Hq * 4 + small
     return float(total), float(flops), float(q_bytes + kv_bytes)
 
@@ -192,9 +195,15 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
         _sync(dist_ctx)
         s0.record(stream)
         for _ in range(steps):
-            B.sinkattn_decode_split(inp["q"], inp["k"], inp["v"], inp["cu_k"], w.q_len, inp["max_k"],
-                                    w.num_kv_heads, run.num_splits, w.scale, w.causal, w.window,
-                                    part_acc=acc, part_md=md)
+            if w.page_size > 0:
+                B.sinkattn_decode_split_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["cu_k"],
+                                              inp["page_indptr"], inp["page_indices"], w.q_len,
+                                              inp["max_k"], run.num_splits, w.scale, w.causal,
+                                              w.window, part_acc=acc, part_md=md)
+            else:
+                B.sinkattn_decode_split(inp["q"], inp["k"], inp["v"], inp["cu_k"], w.q_len,
+                                        inp["max_k"], w.num_kv_heads, run.num_splits, w.scale,
+                                        w.causal, w.window, part_acc=acc, part_md=md)
         s1.record(stream)
         _sync(dist_ctx)
         split_ms = s0.elapsed_time(s1) / steps
@@ -394,9 +403,11 @@ def decode_kernel_name(w):
 
 def _workload_desc(w):
     if w.kind == "decode":
+        layout = ("paged HND bf16, %d-key pages in random order" % w.page_size if w.page_size > 0
+                  else "HND bf16")
         return ("%s: batch %d, %d query / %d KV heads, head_dim %d, q_len %d, kv_len ~ U[%d, %d], "
-                "HND bf16, fp32 sinks" % (w.name, w.batch, w.num_qo_heads, w.num_kv_heads,
-                                          w.head_dim, w.q_len, w.kv_range[0], w.kv_range[1]))
+                "%s, fp32 sinks" % (w.name, w.batch, w.num_qo_heads, w.num_kv_heads,
+                                    w.head_dim, w.q_len, w.kv_range[0], w.kv_range[1], layout))
     return ("%s: seqlens %s, %d query / %d KV heads, head_dim %d, causal, window %d, bf16" % (
         w.name, list(w.kv_lens), w.num_qo_heads, w.num_kv_heads, w.head_dim, w.window))
 

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   const int posN = pos0 + nq - 1;
 
   // Key range [k_lo, k_hi) this CTA must visit.
-  const int chunk = (Lk + S - 1) / S;
+  const int chunk = split_chunk(Lk, S);
   int k_lo = min(split * chunk, Lk);
   int k_hi = min(k_lo + chunk, Lk);
   if (p.causal) k_hi = min(k_hi, posN + 1);
@@ -146,10 +146,12 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   // ------------------------------------------------------------------ producer
   bool writer = false;   // consumer warps holding the CTA's combined state
   if (warp == NW) {
-    // The warp runs the loop (page lists are read 32 entries per warp load);
-    // lane 0 issues every copy.
-    if (ntiles > 0) {
-      const bool leader = (lane == 0);
+    // Contiguous KV: lane 0 runs the loop alone. Paged KV: the whole warp runs
+    // it (page lists are read 32 entries per warp load, lane i issues box i of
+    // a tile).
+    const bool leader = (lane == 0);
+    if (ntiles > 0 && (paged || leader)) {
+      const unsigned members = paged ? 0xffffffffu : 1u;
       if (leader) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
@@ -167,19 +169,17 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NST;
         const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
+        if (!__all_sync(members, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
           break;
         uint8_t* kt = tiles + st * C::STAGE_BYTES;
         uint8_t* vt = kt + C::TILE_BYTES;
         if (leader) mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
         const int j0 = first + i * KT;
         if (!paged) {
-          if (leader) {
 #pragma unroll
-            for (int sub = 0; sub < C::NSUB; ++sub) {
-              tma_load_2d_hint(kt + sub * C::SUB_BYTES, &tmK, sub * 64, slab + j0, &full[st], policy);
-              tma_load_2d_hint(vt + sub * C::SUB_BYTES, &tmV, sub * 64, slab + j0, &full[st], policy);
-            }
+          for (int sub = 0; sub < C::NSUB; ++sub) {
+            tma_load_2d_hint(kt + sub * C::SUB_BYTES, &tmK, sub * 64, slab + j0, &full[st], policy);
+            tma_load_2d_hint(vt + sub * C::SUB_BYTES, &tmV, sub * 64, slab + j0, &full[st], policy);
           }
         } else {
           // one box per page segment, lane i issuing box i: rows (page,

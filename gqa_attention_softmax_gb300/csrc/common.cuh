@@ -164,6 +164,13 @@ __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
   return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
 }
 
+// Split-KV chunk length for Lk keys in S chunks: ceil(Lk / S) rounded up to
+// whole 64-key tiles, so every chunk but the last starts and ends on a tile
+// boundary and no tile is loaded by two chunks.
+__host__ __device__ __forceinline__ int split_chunk(int Lk, int S) {
+  return ((Lk + S - 1) / S + 63) / 64 * 64;
+}
+
 // ---------------------------------------------------------------------------
 // Paged KV: a producer warp's view of one sequence's page list.
 // Entry e of the list (global memory) is the page holding keys

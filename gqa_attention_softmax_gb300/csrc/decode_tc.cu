@@ -68,7 +68,7 @@ struct DtcItem {
 
 // cu_k is read from `cu` (a shared-memory copy when the batch fits, else
 // global memory): every role derives every item's keys from it.
-template <int KT>
+template <int KT, bool PAGED>
 __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* cu, int it) {
   DtcItem t;
   const int S = p.num_splits;
@@ -85,12 +85,12 @@ __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* c
   t.Lk = cu[t.b + 1] - t.k_start;
   t.pos0 = t.Lk - p.q_len + t.q0;
   const int posN = t.pos0 + t.nq - 1;
-  const int chunk = (t.Lk + S - 1) / S;
+  const int chunk = split_chunk(t.Lk, S);
   t.k_lo = min(t.split * chunk, t.Lk);
   t.k_hi = min(t.k_lo + chunk, t.Lk);
   if (p.causal) t.k_hi = min(t.k_hi, posN + 1);
   if (p.window > 0) t.k_lo = max(t.k_lo, t.pos0 - p.window + 1);
-  if (p.page_size > 0) {
+  if (PAGED) {
     const int t0 = t.k_lo / KT * KT;
     t.n = (t.k_hi > t.k_lo) ? (t.k_hi - t0 + KT - 1) / KT : 0;
     t.first = t0;
@@ -154,7 +154,7 @@ struct DtcCfg {
 // as (m', lr) with m' = m + ln(l / lr): m' + ln lr is the chunk's exact
 // log-sum-exp and acc / lr its output normalised by the weights actually
 // applied -- the same state, rescaled, as (chunk max, exact sum).
-template <int RR>
+template <int RR, bool PAGED>
 __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     for (int i = threadIdx.x; i < n_cu; i += blockDim.x) cu_s[i] = p.cu_k[i];
   const int32_t* cu = cu_in_smem ? cu_s : p.cu_k;
   auto item_of = [&](int k) {
-    return dtc_item<KT>(p, cu, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x));
+    return dtc_item<KT, PAGED>(p, cu, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x));
   };
 
   if (threadIdx.x == 0) {
@@ -234,76 +234,81 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
 
   if (warp == 10) {
     // ---------------------------------------------------------------- producer
-    // The warp runs the loop (page lists are read 32 entries per warp load);
-    // lane 0 issues every copy.
+    // Contiguous KV: lane 0 runs the loop alone. Paged KV: the whole warp runs
+    // it (page lists are read 32 entries per warp load, lane i issues box i of
+    // a tile) and lane 0 issues the other copies.
     const bool leader = (lane == 0);
-    if (leader) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
-    const uint64_t policy = policy_evict_first();   // K/V are streamed once
-    const bool paged = p.page_size > 0;
-    PageCursor pc;
-    int g = 0, qi = 0;                               // tile and non-empty item ordinals
-    bool ok = true;
-    for (int k = 0; ok && k < n_mine; ++k) {
-      const DtcItem t = item_of(k);
-      if (leader && (t.Lk < p.q_len || t.Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
-      if (t.n == 0) continue;
-      if (!wwait(&q_empty[qi & 1], ((qi >> 1) & 1) ^ 1)) { ok = false; break; }
+    if (PAGED || leader) {
+      auto pwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if constexpr (PAGED) return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+        else return mbar_wait(bar, parity, abort_flag, status);
+      };
       if (leader) {
-        mbar_arrive_expect_tx(&q_full[qi & 1], static_cast<uint32_t>(2 * 128 * p.G * p.QB));
-        for (int sub = 0; sub < 2; ++sub)
-          tc::tma_load_3d(smem + C::OFF_Q + (qi & 1) * C::Q_BUF + sub * C::Q_SUB, &tmQ, sub * 64,
-                          t.kvh * p.G, t.q_start + t.q0, &q_full[qi & 1]);
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
       }
-      ++qi;
-      if (paged) {
-        const int e0 = p.page_indptr[t.b];
-        const int np = p.page_indptr[t.b + 1] - e0;
-        if (leader && t.Lk > np * p.page_size) atomicExch(status, SINKATTN_BAD_LENGTHS);
-        pc.start(p.page_indices + e0, np, t.first / p.page_size, lane);
-      }
-      const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // contiguous: tensor-map row of key 0
-      for (int j = 0; j < t.n; ++j, ++g) {
-        const int st = g % NST;
-        if (!wwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
-        uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
-        if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-        const int j0 = t.first + j * KT;
-        if (!paged) {
-          if (leader) {
+      const uint64_t policy = policy_evict_first();   // K/V are streamed once
+      [[maybe_unused]] PageCursor pc;
+      int g = 0, qi = 0;                               // tile and non-empty item ordinals
+      bool ok = true;
+      for (int k = 0; ok && k < n_mine; ++k) {
+        const DtcItem t = item_of(k);
+        if (leader && (t.Lk < p.q_len || t.Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
+        if (t.n == 0) continue;
+        if (!pwait(&q_empty[qi & 1], ((qi >> 1) & 1) ^ 1)) { ok = false; break; }
+        if (leader) {
+          mbar_arrive_expect_tx(&q_full[qi & 1], static_cast<uint32_t>(2 * 128 * p.G * p.QB));
+          for (int sub = 0; sub < 2; ++sub)
+            tc::tma_load_3d(smem + C::OFF_Q + (qi & 1) * C::Q_BUF + sub * C::Q_SUB, &tmQ,
+                            sub * 64, t.kvh * p.G, t.q_start + t.q0, &q_full[qi & 1]);
+        }
+        ++qi;
+        if constexpr (PAGED) {
+          const int e0 = p.page_indptr[t.b];
+          const int np = p.page_indptr[t.b + 1] - e0;
+          if (leader && t.Lk > np * p.page_size) atomicExch(status, SINKATTN_BAD_LENGTHS);
+          pc.start(p.page_indices + e0, np, t.first / p.page_size, lane);
+        }
+        const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // contiguous: tensor-map row of key 0
+        for (int j = 0; j < t.n; ++j, ++g) {
+          const int st = g % NST;
+          if (!pwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
+          uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
+          if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+          const int j0 = t.first + j * KT;
+          if constexpr (!PAGED) {
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
-              tma_load_2d_hint(kt + sub * C::SUB_KV, &tmK, sub * 64, slab + j0, &kv_full[st], policy);
+              tma_load_2d_hint(kt + sub * C::SUB_KV, &tmK, sub * 64, slab + j0, &kv_full[st],
+                               policy);
               tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV, &tmV, sub * 64, slab + j0,
                                &kv_full[st], policy);
             }
-          }
-        } else {
-          // one box per page segment, lane i issuing box i: rows (page,
-          // head, slot) of the pool
-          const int nbox = KT / p.box_rows;
-          const int a = j0 + min(lane, nbox - 1) * p.box_rows;
-          const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
-          if (lane < nbox) {
-            const int row = (page * p.Hkv + t.kvh) * p.page_size + a % p.page_size;
-            const int off = (a - j0) * 128;
+          } else {
+            // one box per page segment, lane i issuing box i: rows (page,
+            // head, slot) of the pool
+            const int nbox = KT / p.box_rows;
+            const int a = j0 + min(lane, nbox - 1) * p.box_rows;
+            const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
+            if (lane < nbox) {
+              const int row = (page * p.Hkv + t.kvh) * p.page_size + a % p.page_size;
+              const int off = (a - j0) * 128;
 #pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-              tma_load_2d_hint(kt + sub * C::SUB_KV + off, &tmK, sub * 64, row, &kv_full[st],
-                               policy);
-              tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV + off, &tmV, sub * 64, row,
-                               &kv_full[st], policy);
+              for (int sub = 0; sub < 2; ++sub) {
+                tma_load_2d_hint(kt + sub * C::SUB_KV + off, &tmK, sub * 64, row, &kv_full[st],
+                                 policy);
+                tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB_KV + off, &tmV, sub * 64, row,
+                                 &kv_full[st], policy);
+              }
             }
           }
         }
       }
-    }
-    if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
-      for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
-      for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+      if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
+        for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
+        for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+      }
     }
   } else if (warp == 11) {
     // ---------------------------------------------------------------- MMA issuer
@@ -577,7 +582,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int RR>
+template <int RR, bool PAGED>
 static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
   using C = DtcCfg<RR>;
   const int G = a.Hq / a.Hkv;
@@ -617,7 +622,7 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
   p.window = a.window;
   p.part_acc = a.part_acc;
   p.part_md = a.part_md;
-  auto kern = decode_tc_kernel<RR>;
+  auto kern = decode_tc_kernel<RR, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -647,11 +652,18 @@ int launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   }
   const int QB = min(a.q_len, 128 / G);   // query tokens per CTA
   const int R = G * QB;                   // real rows of the 128-row tile
-  if (R <= 16) return launch_dtc<16>(a, QB, stream);
-  if (R <= 32) return launch_dtc<32>(a, QB, stream);
-  if (R <= 48) return launch_dtc<48>(a, QB, stream);
-  if (R <= 64) return launch_dtc<64>(a, QB, stream);
-  return launch_dtc<128>(a, QB, stream);
+  if (a.page_size > 0) {
+    if (R <= 16) return launch_dtc<16, true>(a, QB, stream);
+    if (R <= 32) return launch_dtc<32, true>(a, QB, stream);
+    if (R <= 48) return launch_dtc<48, true>(a, QB, stream);
+    if (R <= 64) return launch_dtc<64, true>(a, QB, stream);
+    return launch_dtc<128, true>(a, QB, stream);
+  }
+  if (R <= 16) return launch_dtc<16, false>(a, QB, stream);
+  if (R <= 32) return launch_dtc<32, false>(a, QB, stream);
+  if (R <= 48) return launch_dtc<48, false>(a, QB, stream);
+  if (R <= 64) return launch_dtc<64, false>(a, QB, stream);
+  return launch_dtc<128, false>(a, QB, stream);
 }
 
 int read_status_decode_tc(cudaStream_t s, int* status) {

@@ -34,7 +34,8 @@ class Runner:
         # decode: split + merge through a workspace. The cluster-fused form
         # (sinkattn_decode_fused) is available but measured slower on the
         # gpt-oss- and Qwen-shaped decodes, so it is opt-in.
-        self.fused = w.kind == "decode" and fused and self.num_splits <= 16
+        self.fused = (w.kind == "decode" and fused and self.num_splits <= 16
+                      and w.page_size == 0)
         self.workspace = None
         if w.kind == "decode" and not self.fused:
             n = B.sinkattn_decode_workspace_bytes(inp["batch"], w.q_len, w.num_qo_heads, w.head_dim,
@@ -52,6 +53,13 @@ class Runner:
                                            i["max_k"], w.num_kv_heads, num_splits=self.num_splits,
                                            sm_scale=w.scale, causal=w.causal, window=w.window,
                                            out=self.out, lse=self.lse, stream=stream)
+        if w.kind == "decode" and w.page_size > 0:
+            return B.sinkattn_decode_paged(i["q"], i["k_pages"], i["v_pages"], i["cu_k"],
+                                           i["page_indptr"], i["page_indices"], i["sinks"],
+                                           w.q_len, i["max_k"], num_splits=self.num_splits,
+                                           sm_scale=w.scale, causal=w.causal, window=w.window,
+                                           workspace=self.workspace, out=self.out, lse=self.lse,
+                                           stream=stream)
         if w.kind == "decode":
             return B.sinkattn_decode(i["q"], i["k"], i["v"], i["cu_k"], i["sinks"], w.q_len,
                                      i["max_k"], w.num_kv_heads, num_splits=self.num_splits,

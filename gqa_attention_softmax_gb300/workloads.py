@@ -57,6 +57,7 @@ class Workload:
     sink_dist: str = "normal"       # "normal" -> N(0,1); "uniform2" -> U(-2, 2)
     sm_scale: Optional[float] = None  # None -> 1/sqrt(head_dim)
     seed: int = 0
+    page_size: int = 0              # > 0: K/V also scattered into page pools (paged decode)
 
     @property
     def scale(self) -> float:
@@ -85,6 +86,13 @@ WORKLOADS = {
     # Qwen3-235B-shaped MTP speculative decode: 3 drafts, 16 KV chunks.
     "qwen_mtp_decode": Workload("qwen_mtp_decode", "decode", 64, 4, 128, True, batch=256, q_len=3,
                                 kv_range=(4000, 8000), num_splits=16, sink_dist="uniform2"),
+    # The two decodes over a paged KV cache (pages in seeded random order).
+    "gptoss_decode_paged": Workload("gptoss_decode_paged", "decode", 64, 8, 64, True, batch=64,
+                                    q_len=1, kv_range=(1024, 8192), sink_dist="uniform2",
+                                    sm_scale=1.0 / 8.0, page_size=16),
+    "qwen_mtp_decode_paged": Workload("qwen_mtp_decode_paged", "decode", 64, 4, 128, True,
+                                      batch=256, q_len=3, kv_range=(4000, 8000), num_splits=16,
+                                      sink_dist="uniform2", page_size=64),
 }
 
 
@@ -141,13 +149,16 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
     else:
         sinks = torch.randn((Hq,), generator=gen, device=device, dtype=torch.float32)
 
-    return dict(
+    inp = dict(
         q=q, k=k, v=v, sinks=sinks,
         cu_q=torch.tensor(cu_q, dtype=torch.int32, device=device),
         cu_k=torch.tensor(cu_k, dtype=torch.int32, device=device),
         q_lens=q_lens, kv_lens=kv_lens, batch=B, total_q=total_q, total_k=total_k,
         max_q=max(q_lens) if q_lens else 0, max_k=max(kv_lens) if kv_lens else 0,
     )
+    if w.page_size > 0:
+        inp.update(to_paged(inp, Hkv, w.page_size, seed=seed, spare_pages=0, fill_scale=0.0))
+    return inp
 
 
 def explicit_inputs(q_lens, kv_lens, Hq, Hkv, d, seed=0, device="cpu",
@@ -164,36 +175,43 @@ def to_paged(inp: dict, Hkv: int, page_size: int, seed: int = 0, spare_pages: in
     """Scatter the ragged HND ``k``/``v`` of ``inp`` into page pools.
 
     Pages are handed out in a seeded random order (in pool order if not
-    ``shuffle``), plus ``spare_pages`` that no sequence uses; every slot that holds no key of a sequence -- the tail of
-    each sequence's last page and the spare pages -- is filled with large
-    finite values (N(0, fill_scale^2), bf16), so a kernel that lets such a slot
-    through its mask shows it. Returns k_pages, v_pages, page_indptr,
-    page_indices on the device of ``inp["k"]``. Pure data movement.
+    ``shuffle``), plus ``spare_pages`` that no sequence uses; every slot that
+    holds no key of a sequence -- the tail of each sequence's last page and
+    the spare pages -- is filled with large finite values (N(0, fill_scale^2),
+    bf16; zeros if fill_scale is 0), so a kernel that lets such a slot through
+    its mask shows it. Returns k_pages, v_pages, page_indptr, page_indices on
+    the device of ``inp["k"]``. Pure data movement.
     """
     k, v = inp["k"], inp["v"]
     dev = k.device
     d = k.shape[1]
-    kv_lens = list(inp["kv_lens"])
-    n_b = [(L + page_size - 1) // page_size for L in kv_lens]
-    used = sum(n_b)
+    kv_lens = torch.tensor(list(inp["kv_lens"]), dtype=torch.int64)
+    n_b = (kv_lens + page_size - 1) // page_size
+    used = int(n_b.sum())
     total = used + spare_pages
     gen = torch.Generator(device="cpu").manual_seed(seed)
     perm = torch.randperm(total, generator=gen) if shuffle else torch.arange(total)
     shape = (total, Hkv, page_size, d)
-    kp = (torch.randn(shape, generator=gen) * fill_scale).to(torch.bfloat16)
-    vp = (torch.randn(shape, generator=gen) * fill_scale).to(torch.bfloat16)
-    k_cpu, v_cpu = k.cpu(), v.cpu()
-    indptr = [0]
-    r0 = 0
-    for L, n in zip(kv_lens, n_b):
-        idx = perm[indptr[-1]:indptr[-1] + n]
-        for src, pool in ((k_cpu, kp), (v_cpu, vp)):
-            blk = src[r0:r0 + Hkv * L].view(Hkv, L, d)
-            cur = pool[idx].permute(1, 0, 2, 3).reshape(Hkv, n * page_size, d)
-            cur[:, :L] = blk
-            pool[idx] = cur.view(Hkv, n, page_size, d).permute(1, 0, 2, 3)
-        indptr.append(indptr[-1] + n)
-        r0 += Hkv * L
-    return dict(k_pages=kp.to(dev), v_pages=vp.to(dev),
-                page_indptr=torch.tensor(indptr, dtype=torch.int32, device=dev),
+    if fill_scale == 0:
+        kp = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    else:
+        fgen = gen if dev.type == "cpu" else torch.Generator(device=dev).manual_seed(seed)
+        kp = (torch.randn(shape, generator=fgen, device=dev) * fill_scale).to(torch.bfloat16)
+        vp = (torch.randn(shape, generator=fgen, device=dev) * fill_scale).to(torch.bfloat16)
+    indptr = torch.zeros(len(n_b) + 1, dtype=torch.int64)
+    indptr[1:] = torch.cumsum(n_b, 0)
+    # destination row of every source row (sequence b, head h, key t) of the
+    # ragged HND layout: slot t % P of head h in page perm[indptr[b] + t // P]
+    rows_b = Hkv * kv_lens
+    b_of = torch.repeat_interleave(torch.arange(len(kv_lens)), rows_b).to(dev)
+    start = (torch.cumsum(rows_b, 0) - rows_b).to(dev)
+    o = torch.arange(int(rows_b.sum()), device=dev) - start[b_of]
+    L = kv_lens.to(dev)[b_of]
+    h, t = o // L, o % L
+    page = perm.to(dev)[indptr.to(dev)[b_of] + t // page_size]
+    dest = (page * Hkv + h) * page_size + t % page_size
+    kp.view(-1, d)[dest] = k
+    vp.view(-1, d)[dest] = v
+    return dict(k_pages=kp, v_pages=vp, page_indptr=indptr.to(torch.int32).to(dev),
                 page_indices=perm[:used].to(torch.int32).to(dev))

@@ -104,8 +104,10 @@ SINKATTN_API int sinkattn_prefill(const void* q, const void* k, const void* v, c
  *
  *   q [batch*q_len, Hq, d] bf16; k/v ragged HND with kv_indptr [batch+1] (device);
  *   max_kv_len bounds every Lk_b (host); each sequence needs Lk_b >= q_len.
- *   Sequence b's keys are cut into num_splits chunks of c = ceil(Lk_b/num_splits)
- *   keys; chunk s covers [s*c, min((s+1)*c, Lk_b)) and may be empty.
+ *   Sequence b's keys are cut into num_splits chunks of
+ *   c = 64 * ceil(Lk_b / (64 * num_splits)) keys (ceil(Lk_b / num_splits)
+ *   rounded up to whole 64-key tiles); chunk s covers
+ *   [s*c, min((s+1)*c, Lk_b)) and may be empty.
  *   part_md:  fp32 [batch*q_len, Hq, num_splits, 2]: (m_s, d_s), natural
  *             units, with m_s + ln d_s = ln sum_j e^{l_j}, the chunk's
  *             log-sum-exp over its visible keys;

@@ -145,7 +145,8 @@ def split_partials(q, k, v, cu_q, cu_k, num_qo_heads, num_kv_heads, head_dim,
     """Per-chunk (acc, m, d) of the split-KV method, no sink.
 
     Returns acc [total_q, Hq, S, d], m [total_q, Hq, S], d [total_q, Hq, S],
-    all float64, chunks of ceil(Lk_b / S) keys.
+    all float64, chunks of 64 * ceil(Lk_b / (64 S)) keys (the last may be
+    shorter, later ones empty).
     """
     lib = _load()
     qb, kb, vb = _bits(q), _bits(k), _bits(v)

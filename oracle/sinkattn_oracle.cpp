@@ -238,8 +238,9 @@ int oracle_attend_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 }
 
 // Per-chunk partials of the split-KV method, without the sink. Sequence b's
-// keys are cut into num_splits chunks of c = ceil(Lk_b / num_splits) keys;
-// chunk s covers [s*c, min((s+1)*c, Lk_b)) and may be empty.
+// keys are cut into num_splits chunks of c = 64 * ceil(Lk_b / (64 * num_splits))
+// keys (ceil(Lk_b / num_splits) rounded up to whole 64-key tiles); chunk s
+// covers [s*c, min((s+1)*c, Lk_b)) and may be empty.
 //   part_acc: [total_q, Hq, S, d]; part_m, part_d: [total_q, Hq, S].
 int oracle_split_partials(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                           const int32_t* cu_q, const int32_t* cu_k, int B, int Hq,
@@ -256,7 +257,7 @@ int oracle_split_partials(const uint16_t* q, const uint16_t* k, const uint16_t* 
     const int h = static_cast<int>(row % Hq);
     const int b = sequence_of(P, tok);
     const int64_t Lk = cu_k[b + 1] - cu_k[b];
-    const int64_t c = (Lk + S - 1) / S;
+    const int64_t c = 64 * ((Lk + 64 * S - 1) / (64 * S));
     for (int s = 0; s < S; ++s) {
       const int64_t lo = s * c;
       const int64_t hi = (s + 1) * c < Lk ? (s + 1) * c : Lk;

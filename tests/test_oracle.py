@@ -307,9 +307,14 @@ def test_split_invariance_every_partition(oracle_lib, Lk):
 
 
 @pytest.mark.parametrize("S", [1, 2, 3, 7, 16, 40])
-def test_ceil_split_rule_then_merge_equals_unsplit(oracle_lib, S):
+def test_split_rule_then_merge_equals_unsplit(oracle_lib, S):
+    """Chunks of c = 64 * ceil(Lk / (64 S)) keys (ceil(Lk / S) rounded up to a
+    whole number of 64-key tiles): each chunk's partial is the partial of its
+    key range, chunks past the end are empty, and the merge of all chunks is
+    the unsplit result."""
     Hq, Hkv, d = 8, 2, 16
-    inp = workloads.explicit_inputs([3, 1, 2], [3, 17, 33], Hq, Hkv, d, seed=11)
+    kv_lens = [3, 170, 333]
+    inp = workloads.explicit_inputs([3, 1, 2], kv_lens, Hq, Hkv, d, seed=11)
     sinks = np.linspace(-2, 2, Hq)
     acc, m, dd = oracle.split_partials(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"], Hq,
                                        Hkv, d, 0.25, True, 0, S)
@@ -318,12 +323,18 @@ def test_ceil_split_rule_then_merge_equals_unsplit(oracle_lib, S):
                                        inp["cu_k"], Hq, Hkv, d, 0.25, True, 0)
     np.testing.assert_allclose(out.reshape(want_out.shape), want_out, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse.reshape(want_lse.shape), want_lse, rtol=0, atol=1e-12)
-    # chunk sizes follow ceil(Lk/S): chunks past the end are empty
-    for b, Lk in enumerate([3, 17, 33]):
-        c = -(-Lk // S)
-        n_nonempty = len([s for s in range(S) if s * c < Lk])
+    args = (inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"], Hq, Hkv, d, 0.25, True, 0)
+    for b, Lk in enumerate(kv_lens):
+        c = 64 * (-(-Lk // (64 * S)))
+        assert c % 64 == 0 and c * S >= Lk and (c - 64) * S < Lk
         tok = [2, 3, 5][b]   # last query of each sequence sees every key
-        assert np.isfinite(m[tok, 0]).sum() == n_nonempty
+        for s in range(S):
+            lo, hi = min(s * c, Lk), min((s + 1) * c, Lk)
+            for h in (0, Hq - 1):
+                a1, m1, d1 = oracle.chunk_partial(*args, tok * Hq + h, lo, hi)
+                assert (m[tok, h, s] == m1) and (dd[tok, h, s] == d1)
+                np.testing.assert_array_equal(acc[tok, h, s], a1)
+            assert np.isfinite(m[tok, 0, s]) == (lo < hi)
 
 
 def test_merge_is_invariant_to_rescaled_partials(oracle_lib):
