@@ -22,16 +22,16 @@
 //    issues back to back;
 //    with S_t = Q_t K^T (M 128, N 128, K d; both operands in shared memory)
 //    and O_t += P_t V (M 128, N d, K 128; P_t read from TMEM, V from shared);
-//  * warps 2-9 / 10-17: softmax of tile A / B, two threads per row (= TMEM
-//    lane), one per 64-column half of S. The running max starts at the head's
-//    sink and the running sum at 1 ("GPT-OSS on Day 0", section "Kernels for
-//    GPT-OSS / Sink attention"). Each thread loads its 64 scores from TMEM in
-//    one batch; the halves exchange row maxima through shared memory (an
-//    mbarrier with a bounded wait); P goes back as bf16 into the first 64
-//    columns of the same TMEM region. O_t is rescaled in TMEM when a row's
-//    maximum grows; the previous PV_t has completed by then, because S_t(j)
-//    is only issued after it. Row sums are kept both exact (for
-//    lse) and over the bf16-rounded weights the MMA applies (for out). With
+//  * warps 2-5 / 6-9: softmax of tile A / B, one thread per row (= TMEM
+//    lane). The running max starts at the head's sink and the running sum at
+//    1 ("GPT-OSS on Day 0", section "Kernels for GPT-OSS / Sink attention").
+//    Each thread loads its row's 128 scores from TMEM in one batch, so the
+//    row maximum and sums need no exchange between threads; P goes back as
+//    bf16 into the first 64 columns of the same TMEM region. O_t is rescaled
+//    in TMEM when a row's maximum grows; the previous PV_t has completed by
+//    then, because S_t(j) is only issued after it. Row sums are kept both
+//    exact (for lse) and over the bf16-rounded weights the MMA applies (for
+//    out). With
 //    d = 64 the second sum comes from the tensor core: the P.V MMA is 80
 //    columns wide, its extra 16 columns multiplying P by a shared-memory block
 //    of bf16 ones, so O_t's column 64 holds exactly the sum of the weights the
@@ -75,11 +75,10 @@ struct TcCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
   static constexpr int OFF_ONES = OFF_KV + NST * STAGE;   // [128][64] bf16 ones (SUMCOL)
-  static constexpr int OFF_XCH = OFF_ONES + (SUMCOL ? SUB : 0);   // [2][2][128][2] floats
-  static constexpr int OFF_BAR = OFF_XCH + 2 * 2 * 128 * 2 * 4;
-  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + 2 + 1;
+  static constexpr int OFF_BAR = OFF_ONES + (SUMCOL ? SUB : 0);
+  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
-  static constexpr int THREADS = 576;             // TMA, MMA, 2 tiles x 2 halves x 4 softmax warps
+  static constexpr int THREADS = 320;             // TMA, MMA, 2 tiles x 4 softmax warps
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S_t (P_t in its first 64 columns) at 128 t, O_t at 256 + NO t.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
@@ -88,7 +87,7 @@ struct TcCfg {
 };
 
 template <int D, int NST>
-__global__ void __launch_bounds__(576, 1)
+__global__ void __launch_bounds__(320, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
@@ -103,11 +102,9 @@ __global__ void __launch_bounds__(576, 1)
   uint64_t* kv_full = q_full + 1;
   uint64_t* kv_empty = kv_full + NST;
   uint64_t* s_full = kv_empty + NST;   // [2]: S_t(j) written
-  uint64_t* p_full = s_full + 2;       // [2]: P_t(j) written and O_t rescaled (256 arrivals)
+  uint64_t* p_full = s_full + 2;       // [2]: P_t(j) written and O_t rescaled (128 arrivals)
   uint64_t* pv_done = p_full + 2;      // [2]: PV_t(j) completed
-  uint64_t* xch = pv_done + 2;         // [2]: the halves of tile t exchanged (256 arrivals)
-  uint64_t* drain = xch + 2;
-  float* xch_mem = reinterpret_cast<float*>(smem + C::OFF_XCH);
+  uint64_t* drain = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* status = &g_status_prefill_tc;
@@ -147,9 +144,8 @@ __global__ void __launch_bounds__(576, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 256);
+      mbar_init(&p_full[t], 128);
       mbar_init(&pv_done[t], 1);
-      mbar_init(&xch[t], 256);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -325,10 +321,8 @@ __global__ void __launch_bounds__(576, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    // 16 warps: tile t = A/B, column half hf of S_t, TMEM lane quadrant.
-    const int sw = warp - 2;
-    const int t = sw >> 3;
-    const int hf = (sw >> 2) & 1;
+    // 8 warps: tile t = A/B; warp w may access TMEM lanes 32 (w % 4) ...
+    const int t = (warp - 2) >> 2;
     const int quad = warp & 3;       // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const int G = p.G;
@@ -342,21 +336,17 @@ __global__ void __launch_bounds__(576, 1)
     if (p.window > 0) lo_r = max(lo_r, pos - p.window + 1);
     if (p.causal) hi_r = min(hi_r, pos);
     const float c2 = p.scale_log2;
-    float* my_x = xch_mem + ((t * 2 + hf) * 128 + row) * 2;
-    const float* other_x = xch_mem + ((t * 2 + (hf ^ 1)) * 128 + row) * 2;
 
-    // Both halves track the same running maximum. l: this half's exact
-    // running sum (for lse); lr: this half's sum of the bf16-rounded weights
-    // the P.V MMA applies (for out) -- with the sum column the MMA provides
-    // the row's sum and lr holds only the sink's weight. The sink's own term
-    // is counted by half 0.
+    // l: the row's exact running sum (for lse); lr: its sum of the
+    // bf16-rounded weights the P.V MMA applies (for out) -- with the sum
+    // column the MMA provides that sum and lr holds only the sink's weight.
     float m_used = kNegInf, l = 0.f, lr = 0.f;
     if (p.sinks != nullptr && valid) {
       const float s = p.sinks[h];
       if (s != kNegInf) {
         m_used = s / p.sm_scale;   // the sink, in raw logit units
-        if (hf == 0 || C::SUMCOL) lr = 1.f;
-        if (hf == 0) l = 1.f;
+        lr = 1.f;
+        l = 1.f;
       }
     }
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
@@ -369,22 +359,21 @@ __global__ void __launch_bounds__(576, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
     };
 
-    int xph = 0;   // phases completed on xch[t]
     for (int j = 0; j < n; ++j) {
       if (!wwait(&s_full[t], j & 1)) { ok = false; break; }
       tc::fence_after_sync();
       const int j0 = first + j * KT;
       const bool masked = (j0 < lo_r || j0 + KT - 1 > hi_r);
-      const int clo = lo_r - j0 - 64 * hf, chi = hi_r - j0 - 64 * hf;
+      const int clo = lo_r - j0, chi = hi_r - j0;
 
-      // this half's 64 scores, one batch of loads
-      float v[2][32];
-      tc::tmem_ld32(s_addr + 64 * hf, v[0]);
-      tc::tmem_ld32(s_addr + 64 * hf + 32, v[1]);
+      // the row's 128 scores, one batch of loads
+      float v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_addr + 32 * c, v[c]);
       tc::tmem_wait_ld();
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
           const int lo_c = clo - c * 32, hi_c = chi - c * 32;
           if (lo_c <= 0 && hi_c >= 31) continue;
 #pragma unroll
@@ -392,18 +381,19 @@ __global__ void __launch_bounds__(576, 1)
             if (e < lo_c || e > hi_c) v[c][e] = kNegInf;
         }
       }
-      float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+      // row maximum: 8 independent chains of three-input maxima
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(v[i >> 1][(i & 1) * 16], v[i >> 1][(i & 1) * 16 + 1]);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mx4[(e >> 1) & 3] = fmax3(mx4[(e >> 1) & 3], v[c][e], v[c][e + 1]);
-      // row maximum across the two halves
-      my_x[0] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      mbar_arrive(&xch[t]);
-      if (!wwait(&xch[t], xph & 1)) { ok = false; break; }
-      ++xph;
-      const float mx = fmaxf(my_x[0], other_x[0]);
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 2; e < 16; e += 2) {
+          mx8[2 * c] = fmax3(mx8[2 * c], v[c][e], v[c][e + 1]);
+          mx8[2 * c + 1] = fmax3(mx8[2 * c + 1], v[c][16 + e], v[c][16 + e + 1]);
+        }
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
 
       float alpha = 1.f;
       bool rescale = false;
@@ -414,40 +404,46 @@ __global__ void __launch_bounds__(576, 1)
       }
       const float mb = (m_used == kNegInf) ? 0.f : m_used * c2;
 
-      // P = 2^(s*c2 - mb) as bf16: this half's keys go to P columns
-      // [32 hf, 32 hf + 32) of S_t, which only hold scores already loaded (by
-      // this half, or by half 0 before the exchange above).
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(s*c2 - mb) as bf16 into P columns [0, 64) of S_t (all 128
+      // scores are already in registers). Scale-subtract and the exact sum
+      // run two lanes per instruction (paired fp32 FMA / add).
+      const float2 c2x2 = make_float2(c2, c2), nmb2 = make_float2(-mb, -mb);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a0 = ex2(fmaf(v[c][e], c2, -mb));
-          const float a1 = ex2(fmaf(v[c][e + 1], c2, -mb));
-          rs4[(e >> 1) & 3] += a0 + a1;
-          pk[e >> 1] = pack_bf16x2(a0, a1);
-          if (!C::SUMCOL) rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const int k = hh * 16 + e;
+            const float2 x = __ffma2_rn(make_float2(v[c][k], v[c][k + 1]), c2x2, nmb2);
+            const float2 a = make_float2(ex2(x.x), ex2(x.y));
+            rs2[(e >> 1) & 3] = __fadd2_rn(rs2[(e >> 1) & 3], a);
+            pk[e >> 1] = pack_bf16x2(a.x, a.y);
+            if (!C::SUMCOL) rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+          }
+          tc::tmem_st8(s_addr + 16 * c + 8 * hh, pk);
         }
-        tc::tmem_st16(s_addr + 32 * hf + 16 * c, pk);
-      }
-      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+      const float rs = rsa.x + rsa.y;
       const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
 
-      // Rescale this half's columns of O_t when some row of this warp moved
-      // its maximum (warp-uniform; both halves see the same rows move).
+      // Rescale the row's O_t when some row of this warp moved its maximum
+      // (warp-uniform branch).
       if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tc::tmem_ld32(o_addr + (D / 2) * hf + c * 32, o);
+          tc::tmem_ld32(o_addr + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc::tmem_st32(o_addr + (D / 2) * hf + c * 32, o);
+          tc::tmem_st32(o_addr + c * 32, o);
         }
-        if (C::SUMCOL && hf == 1) {
+        if (C::SUMCOL) {
           float o[16];
           tc::tmem_ld16(o_addr + D, o);
           tc::tmem_wait_ld();
@@ -468,18 +464,7 @@ __global__ void __launch_bounds__(576, 1)
       ok = wwait(&pv_done[t], (n - 1) & 1);
       tc::fence_after_sync();
     }
-    // combine the halves' sums
-    if (ok) {
-      my_x[0] = l;
-      my_x[1] = lr;
-      mbar_arrive(&xch[t]);
-      ok = wwait(&xch[t], xph & 1);
-    }
-    float l_tot = l, lr_tot = lr;
-    if (ok) {
-      l_tot = l + other_x[0];
-      lr_tot = C::SUMCOL ? lr : lr + other_x[1];
-    }
+    float lr_tot = lr;
     if (C::SUMCOL && n >= 1 && ok) {
       float o[16];
       tc::tmem_ld16(o_addr + D, o);
@@ -487,12 +472,12 @@ __global__ void __launch_bounds__(576, 1)
       lr_tot += o[0];
     }
     const float inv = lr_tot > 0.f ? 1.f / lr_tot : 0.f;
-    __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D + (D / 2) * hf;
+    __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       float o[32];
       if (n >= 1 && ok) {
-        tc::tmem_ld32(o_addr + (D / 2) * hf + c * 32, o);
+        tc::tmem_ld32(o_addr + c * 32, o);
         tc::tmem_wait_ld();
       } else {
 #pragma unroll
@@ -510,9 +495,9 @@ __global__ void __launch_bounds__(576, 1)
         }
       }
     }
-    if (valid && hf == 0 && p.lse != nullptr)
+    if (valid && p.lse != nullptr)
       p.lse[static_cast<size_t>(tok) * p.Hq + h] =
-          l_tot > 0.f ? (m_used * c2 + lg2(l_tot)) * kLn2 : kNegInf;
+          l > 0.f ? (m_used * c2 + lg2(l)) * kLn2 : kNegInf;
   }
 
   tc::fence_before_sync();
