@@ -180,10 +180,8 @@ __host__ __device__ __forceinline__ int split_chunk(int Lk, int S) {
 // masked wherever they fall outside the sequence); an empty list reads page 0
 // (the caller records the length error). get() is warp-collective: it moves
 // the cursor to entry `e_first` (non-decreasing across calls) and returns to
-// each lane the page of its own entry `e`, which must lie in the same aligned
-// group of 32 entries as e_first -- true for the entries of one KV tile, whose
-// KT / page_size pages (a power of two up to 8) start on a multiple of that
-// count.
+// each lane the page of its own entry `e`, which must lie in
+// [e_first, e_first + 32) -- the entries of one KV tile (at most 8).
 // ---------------------------------------------------------------------------
 struct PageCursor {
   const int32_t* list;
@@ -204,7 +202,9 @@ struct PageCursor {
       cur = nxt;
       nxt = load(base + 32 + lane);
     }
-    return __shfl_sync(0xffffffffu, cur, e - base);
+    const int from_cur = __shfl_sync(0xffffffffu, cur, (e - base) & 31);
+    const int from_nxt = __shfl_sync(0xffffffffu, nxt, (e - base) & 31);
+    return e - base < 32 ? from_cur : from_nxt;
   }
 };
 

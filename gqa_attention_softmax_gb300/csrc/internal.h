@@ -43,8 +43,13 @@ inline uint64_t kv_map_rows(const AttnArgs& a) {
   return a.page_size > 0 ? static_cast<uint64_t>(a.num_pages) * a.Hkv * a.page_size
                          : static_cast<uint64_t>(a.Hkv) * a.batch * a.max_kv;
 }
+// Paged KV: boxes of min(page_size, the largest power of two dividing the
+// tile) rows, so a box starting on a multiple of its height never crosses a
+// page; contiguous KV: one box per tile.
 inline int kv_box_rows(const AttnArgs& a, int tile_keys) {
-  return (a.page_size > 0 && a.page_size < tile_keys) ? a.page_size : tile_keys;
+  if (a.page_size <= 0) return tile_keys;
+  const int pow2 = tile_keys & -tile_keys;
+  return a.page_size < pow2 ? a.page_size : pow2;
 }
 
 // Encodes a 2-D tensor map over a [rows, d] bf16 buffer with [box_rows, 64]

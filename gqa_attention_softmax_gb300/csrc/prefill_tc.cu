@@ -64,26 +64,37 @@ struct TcParams {
 
 template <int D, int NST>
 struct TcCfg {
-  static constexpr bool SUMCOL = (D == 64);       // row sums from the tensor core
-  static constexpr int NO = D + (SUMCOL ? 16 : 0);  // O_t columns
+  // d 64: four S buffers shared round-robin by the two tiles, so S is issued
+  // three steps ahead of the P.V that frees its buffer and the tensor core
+  // always has queued work; d 128: one S buffer per tile (no room for more).
+  static constexpr bool RING = (D == 64);
+  static constexpr int NO = D;                    // O_t columns
   static constexpr int NSUB = D / 64;
-  static constexpr int KT = 128;                  // keys per KV tile
-  static constexpr int SUB = 128 * 128;           // [128 rows][64 bf16], 128B-swizzled: 16 KB
-  static constexpr int Q_TILE = NSUB * SUB;
-  static constexpr int KV_TILE = NSUB * SUB;
+  static constexpr int KT = RING ? 96 : 128;      // keys per KV tile
+  static constexpr int NSB = RING ? 4 : 2;        // S buffers
+  static constexpr int QSUB = 128 * 128;          // [128 rows][64 bf16], 128B-swizzled: 16 KB
+  static constexpr int KVSUB = KT * 128;          // [KT rows][64 bf16], 128B-swizzled
+  static constexpr int Q_TILE = NSUB * QSUB;
+  static constexpr int KV_TILE = NSUB * KVSUB;
   static constexpr int STAGE = 2 * KV_TILE;       // K and V of one KV tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
-  static constexpr int OFF_ONES = OFF_KV + NST * STAGE;   // [128][64] bf16 ones (SUMCOL)
-  static constexpr int OFF_BAR = OFF_ONES + (SUMCOL ? SUB : 0);
-  static constexpr int N_BARS = 1 + 2 * NST + 2 + 2 + 2 + 1;
+  static constexpr int OFF_BAR = OFF_KV + NST * STAGE;
+  static constexpr int N_BARS = 1 + 2 * NST + NSB + 2 + 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
   static constexpr int THREADS = 320;             // TMA, MMA, 2 tiles x 4 softmax warps
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns: S_t (P_t in its first 64 columns) at 128 t, O_t at 256 + NO t.
-  __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(NO) * t; }
-  static_assert(256 + 2 * NO <= 512, "TMEM budget");
+  // TMEM columns: S buffers (P in the first KT / 2 columns of its S) at KT b,
+  // O_t after them.
+  __host__ __device__ static constexpr uint32_t col_s(int buf) { return static_cast<uint32_t>(KT) * buf; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) {
+    return static_cast<uint32_t>(NSB * KT + NO * t);
+  }
+  // S buffer of tile t at KV tile j, and how many times it was filled before
+  __host__ __device__ static constexpr int buf_of(int t, int j) { return RING ? (2 * j + t) % NSB : t; }
+  __host__ __device__ static constexpr int use_of(int t, int j) { return RING ? (2 * j + t) / NSB : j; }
+  static_assert(NSB * KT + 2 * NO <= 512, "TMEM budget");
+  static_assert(KVSUB % 1024 == 0 && KT % 32 == 0, "tile shape");
 };
 
 template <int D, int NST>
@@ -101,8 +112,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = q_full + 1;
   uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;   // [2]: S_t(j) written
-  uint64_t* p_full = s_full + 2;       // [2]: P_t(j) written and O_t rescaled (128 arrivals)
+  uint64_t* s_full = kv_empty + NST;   // [NSB]: S written into buffer b
+  uint64_t* p_full = s_full + C::NSB;  // [2]: P_t(j) written and O_t rescaled (128 arrivals)
   uint64_t* pv_done = p_full + 2;      // [2]: PV_t(j) completed
   uint64_t* drain = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -142,8 +153,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
+    for (int i = 0; i < C::NSB; ++i) mbar_init(&s_full[i], 1);
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
       mbar_init(&pv_done[t], 1);
     }
@@ -154,12 +165,6 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc::tmem_relinquish();
-  }
-  if (C::SUMCOL) {
-    uint4* ones = reinterpret_cast<uint4*>(smem + C::OFF_ONES);
-    const uint4 v1 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    for (int i = threadIdx.x; i < C::SUB / 16; i += blockDim.x) ones[i] = v1;
-    tc::fence_proxy_async_smem();   // read by the tensor core
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int sub = 0; sub < C::NSUB; ++sub)
-          tc::tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + sub * C::SUB, &tmQ, sub * 64,
+          tc::tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + sub * C::QSUB, &tmQ, sub * 64,
                           kvh * p.G, q_start + q0 + t * p.QB, q_full);
     }
     const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
@@ -205,8 +210,8 @@ __global__ void __launch_bounds__(320, 1)
         if (leader) {
 #pragma unroll
           for (int sub = 0; sub < C::NSUB; ++sub) {
-            tma_load_2d_hint(kt + sub * C::SUB, &tmK, sub * 64, slab + j0, &kv_full[st], policy);
-            tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB, &tmV, sub * 64, slab + j0,
+            tma_load_2d_hint(kt + sub * C::KVSUB, &tmK, sub * 64, slab + j0, &kv_full[st], policy);
+            tma_load_2d_hint(kt + C::KV_TILE + sub * C::KVSUB, &tmV, sub * 64, slab + j0,
                              &kv_full[st], policy);
           }
         }
@@ -221,8 +226,8 @@ __global__ void __launch_bounds__(320, 1)
           const int off = (a - j0) * 128;
 #pragma unroll
           for (int sub = 0; sub < C::NSUB; ++sub) {
-            tma_load_2d_hint(kt + sub * C::SUB + off, &tmK, sub * 64, row, &kv_full[st], policy);
-            tma_load_2d_hint(kt + C::KV_TILE + sub * C::SUB + off, &tmV, sub * 64, row,
+            tma_load_2d_hint(kt + sub * C::KVSUB + off, &tmK, sub * 64, row, &kv_full[st], policy);
+            tma_load_2d_hint(kt + C::KV_TILE + sub * C::KVSUB + off, &tmV, sub * 64, row,
                              &kv_full[st], policy);
           }
         }
@@ -246,38 +251,37 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, C::NO, true);
       constexpr uint64_t STAGE16 = C::STAGE >> 4;   // one K/V stage, in descriptor address units
-      constexpr uint64_t SUB16 = C::SUB >> 4;
+      constexpr uint64_t QSUB16 = C::QSUB >> 4;
+      constexpr uint64_t KVSUB16 = C::KVSUB >> 4;
       // Descriptors prepared once: a K step (16 elements = 32 bytes) within a
       // 128-byte swizzle row adds 2 to the address field, the next 64-column
-      // block adds SUB / 16, a stage adds STAGE / 16, 16 keys of V add 128.
+      // block adds its size / 16, a stage adds STAGE / 16, 16 keys of V add 128.
       const uint64_t qd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
       const uint64_t kd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
-      // V's second 64-column block: its own (d = 128) or the ones block. The
-      // leading-dimension field then shrinks by one stage per stage.
+      // V is MN-major: its 64-column blocks are KVSUB bytes apart.
       const uint32_t v_base0 = smem_u32(smem + C::OFF_KV + C::KV_TILE);
-      const uint32_t lbo0 = C::SUMCOL ? smem_u32(smem + C::OFF_ONES) - v_base0
-                                      : static_cast<uint32_t>(C::SUB);
-      const uint64_t vd0 = tc::smem_desc_sw128(v_base0, lbo0, 1024);
+      const uint64_t vd0 = tc::smem_desc_sw128(v_base0, static_cast<uint32_t>(C::KVSUB), 1024);
       auto issue_s = [&](int t, int j) {
+        const int buf = C::buf_of(t, j);
         const uint64_t kd = kd0 + static_cast<uint64_t>(j % NST) * STAGE16;
         const uint64_t qd = qd0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
-        const uint32_t d_tm = tmem + C::col_s(t);
+        const uint32_t d_tm = tmem + C::col_s(buf);
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(kk >> 2) * SUB16 + static_cast<uint64_t>(kk & 3) * 2;
-            tc::mma_ss(d_tm, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+            const uint64_t step = static_cast<uint64_t>(kk & 3) * 2;
+            tc::mma_ss(d_tm, qd + static_cast<uint64_t>(kk >> 2) * QSUB16 + step,
+                       kd + static_cast<uint64_t>(kk >> 2) * KVSUB16 + step, idesc_s,
+                       kk > 0 ? 1u : 0u);
           }
-          tc::commit(&s_full[t]);
+          tc::commit(&s_full[buf]);
         }
         __syncwarp();
       };
       auto issue_pv = [&](int t, int j) {
-        const uint64_t st = static_cast<uint64_t>(j % NST);
-        const uint64_t vd = C::SUMCOL ? vd0 + st * STAGE16 - (st * STAGE16 << 16)
-                                      : vd0 + st * STAGE16;
+        const uint64_t vd = vd0 + static_cast<uint64_t>(j % NST) * STAGE16;
         const uint32_t d_tm = tmem + C::col_o(t);
-        const uint32_t a_tm = tmem + C::col_s(t);
+        const uint32_t a_tm = tmem + C::col_s(C::buf_of(t, j));
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
@@ -287,6 +291,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
       };
+      // Order, one buffer per tile: S_A(0) S_B(0), then per KV tile j and
+      // tile t: PV_t(j), then S_t(j+1) into the same buffer once PV_t(j) is
+      // done (the tensor core may not overwrite P before the MMA has read it).
+      // Ring of four, with k = 2 j + t the step's rank: S(0) S(1) S(2), then
+      // per step PV(k), then S(k + 3) into the buffer of PV(k - 1) once that
+      // is done -- PV(k) is queued meanwhile, so the tensor core never drains.
       bool ok = wwait1(q_full, 0);
       if (ok && n > 0) {
         ok = wwait1(&kv_full[0], 0);
@@ -294,6 +304,13 @@ __global__ void __launch_bounds__(320, 1)
           tc::fence_after_sync();
           issue_s(0, 0);
           issue_s(1, 0);
+        }
+        if (ok && C::RING && n > 1) {
+          ok = wwait1(&kv_full[1 % NST], (1 / NST) & 1);
+          if (ok) {
+            tc::fence_after_sync();
+            issue_s(0, 1);
+          }
         }
       }
       for (int j = 0; ok && j < n; ++j) {
@@ -305,12 +322,23 @@ __global__ void __launch_bounds__(320, 1)
             if (leader) tc::commit(&kv_empty[j % NST]);
             __syncwarp();
           }
-          if (j + 1 < n) {
-            if (t == 0 && !wwait1(&kv_full[(j + 1) % NST], ((j + 1) / NST) & 1)) { ok = false; break; }
-            // S_t(j+1) overwrites P_t(j): wait until PV_t(j) has read it.
-            if (!wwait1(&pv_done[t], j & 1)) { ok = false; break; }
+          const int tn = C::RING ? 1 - t : t;
+          const int jn = C::RING ? j + 1 + t : j + 1;
+          if (jn < n) {
+            // a tile's first S of KV tile jn waits for its K
+            if (tn == 0 && !wwait1(&kv_full[jn % NST], (jn / NST) & 1)) { ok = false; break; }
+            // the PV whose buffer the next S overwrites: PV_t(j) with one
+            // buffer per tile; with the ring, the step before (PV_B(j-1) or
+            // PV_A(j))
+            if (!C::RING) {
+              if (!wwait1(&pv_done[t], j & 1)) { ok = false; break; }
+            } else if (t == 1) {
+              if (!wwait1(&pv_done[0], j & 1)) { ok = false; break; }
+            } else if (j >= 1) {
+              if (!wwait1(&pv_done[1], (j - 1) & 1)) { ok = false; break; }
+            }
             tc::fence_after_sync();
-            issue_s(t, j + 1);
+            issue_s(tn, jn);
           }
         }
       }
@@ -337,21 +365,20 @@ __global__ void __launch_bounds__(320, 1)
     if (p.causal) hi_r = min(hi_r, pos);
     const float c2 = p.scale_log2;
 
-    // l: the row's exact running sum (for lse); lr: its sum of the
-    // bf16-rounded weights the P.V MMA applies (for out) -- with the sum
-    // column the MMA provides that sum and lr holds only the sink's weight.
-    float m_used = kNegInf, l = 0.f, lr = 0.f;
+    // l: the row's running sum, the sink's term included (for out and lse).
+    // The running maximum is exact, so the row's largest weight is exactly 1
+    // and the P.V MMA's bf16 rounding of the others stays below 2^-8 of each.
+    float m_used = kNegInf, l = 0.f;
     if (p.sinks != nullptr && valid) {
       const float s = p.sinks[h];
       if (s != kNegInf) {
         m_used = s / p.sm_scale;   // the sink, in raw logit units
-        lr = 1.f;
         l = 1.f;
       }
     }
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t s_addr = lane_base + C::col_s(t);
     const uint32_t o_addr = lane_base + C::col_o(t);
+    constexpr int NCH = KT / 32;     // 32-column chunks of a score row
     bool ok = true;
     // A wait that gives up in any lane makes the whole warp leave, so the
     // warp-collective TMEM loads/stores below never run with missing lanes.
@@ -360,20 +387,22 @@ __global__ void __launch_bounds__(320, 1)
     };
 
     for (int j = 0; j < n; ++j) {
-      if (!wwait(&s_full[t], j & 1)) { ok = false; break; }
+      const int buf = C::buf_of(t, j);
+      if (!wwait(&s_full[buf], C::use_of(t, j) & 1)) { ok = false; break; }
       tc::fence_after_sync();
+      const uint32_t s_addr = lane_base + C::col_s(buf);
       const int j0 = first + j * KT;
       const bool masked = (j0 < lo_r || j0 + KT - 1 > hi_r);
       const int clo = lo_r - j0, chi = hi_r - j0;
 
-      // the row's 128 scores, one batch of loads
-      float v[4][32];
+      // the row's KT scores, one batch of loads
+      float v[NCH][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_addr + 32 * c, v[c]);
+      for (int c = 0; c < NCH; ++c) tc::tmem_ld32(s_addr + 32 * c, v[c]);
       tc::tmem_wait_ld();
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < NCH; ++c) {
           const int lo_c = clo - c * 32, hi_c = chi - c * 32;
           if (lo_c <= 0 && hi_c >= 31) continue;
 #pragma unroll
@@ -381,19 +410,22 @@ __global__ void __launch_bounds__(320, 1)
             if (e < lo_c || e > hi_c) v[c][e] = kNegInf;
         }
       }
-      // row maximum: 8 independent chains of three-input maxima
-      float mx8[8];
+      // row maximum: 2 NCH independent chains of three-input maxima
+      float mxc[2 * NCH];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(v[i >> 1][(i & 1) * 16], v[i >> 1][(i & 1) * 16 + 1]);
+      for (int i = 0; i < 2 * NCH; ++i)
+        mxc[i] = fmaxf(v[i >> 1][(i & 1) * 16], v[i >> 1][(i & 1) * 16 + 1]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int e = 2; e < 16; e += 2) {
-          mx8[2 * c] = fmax3(mx8[2 * c], v[c][e], v[c][e + 1]);
-          mx8[2 * c + 1] = fmax3(mx8[2 * c + 1], v[c][16 + e], v[c][16 + e + 1]);
+          mxc[2 * c] = fmax3(mxc[2 * c], v[c][e], v[c][e + 1]);
+          mxc[2 * c + 1] = fmax3(mxc[2 * c + 1], v[c][16 + e], v[c][16 + e + 1]);
         }
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                             fmaxf(mx8[6], mx8[7]));
+      float mx = fmax3(mxc[0], mxc[1], mxc[2]);
+#pragma unroll
+      for (int i = 3; i < 2 * NCH; i += 2)
+        mx = (i + 1 < 2 * NCH) ? fmax3(mx, mxc[i], mxc[i + 1]) : fmaxf(mx, mxc[i]);
 
       float alpha = 1.f;
       bool rescale = false;
@@ -404,15 +436,14 @@ __global__ void __launch_bounds__(320, 1)
       }
       const float mb = (m_used == kNegInf) ? 0.f : m_used * c2;
 
-      // P = 2^(s*c2 - mb) as bf16 into P columns [0, 64) of S_t (all 128
-      // scores are already in registers). Scale-subtract and the exact sum
-      // run two lanes per instruction (paired fp32 FMA / add).
+      // P = 2^(s*c2 - mb) as bf16 into the first KT / 2 columns of this S
+      // buffer (all KT scores are already in registers). Scale-subtract and
+      // the exact sum run two lanes per instruction (paired fp32 FMA / add).
       const float2 c2x2 = make_float2(c2, c2), nmb2 = make_float2(-mb, -mb);
       float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
-      float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[8];
@@ -423,14 +454,19 @@ __global__ void __launch_bounds__(320, 1)
             const float2 a = make_float2(ex2(x.x), ex2(x.y));
             rs2[(e >> 1) & 3] = __fadd2_rn(rs2[(e >> 1) & 3], a);
             pk[e >> 1] = pack_bf16x2(a.x, a.y);
-            if (!C::SUMCOL) rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
           }
           tc::tmem_st8(s_addr + 16 * c + 8 * hh, pk);
         }
       const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
       const float rs = rsa.x + rsa.y;
-      const float rr = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
 
+      // Ring: PV_t(j-1) has completed before O_t is touched or P_t(j) is
+      // handed over (so p_full[t] cannot run two phases ahead of the MMA
+      // warp). With one buffer per tile S_t(j) was issued after PV_t(j-1).
+      if (C::RING && j >= 1) {
+        if (!wwait(&pv_done[t], (j - 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+      }
       // Rescale the row's O_t when some row of this warp moved its maximum
       // (warp-uniform branch).
       if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
@@ -443,18 +479,9 @@ __global__ void __launch_bounds__(320, 1)
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
           tc::tmem_st32(o_addr + c * 32, o);
         }
-        if (C::SUMCOL) {
-          float o[16];
-          tc::tmem_ld16(o_addr + D, o);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          tc::tmem_st16f(o_addr + D, o);
-        }
       }
       tc::tmem_wait_st();
       l = l * alpha + rs;
-      lr = lr * alpha + rr;
       tc::fence_before_sync();
       mbar_arrive(&p_full[t]);
     }
@@ -464,14 +491,7 @@ __global__ void __launch_bounds__(320, 1)
       ok = wwait(&pv_done[t], (n - 1) & 1);
       tc::fence_after_sync();
     }
-    float lr_tot = lr;
-    if (C::SUMCOL && n >= 1 && ok) {
-      float o[16];
-      tc::tmem_ld16(o_addr + D, o);
-      tc::tmem_wait_ld();
-      lr_tot += o[0];
-    }
-    const float inv = lr_tot > 0.f ? 1.f / lr_tot : 0.f;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
