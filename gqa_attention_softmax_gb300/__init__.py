@@ -6,7 +6,8 @@ Public API (thin wrappers over the C ABI in ``include/sinkattn.h``):
 ``sinkattn_decode_default_splits``, ``sinkattn_prefill_paged``,
 ``sinkattn_decode_split_paged``, ``sinkattn_decode_paged`` (paged KV cache),
 ``sinkattn_status_string``,
-``sinkattn_last_error``, ``sinkattn_debug_status``, ``sinkattn_set_decode_kernel``.
+``sinkattn_last_error``, ``sinkattn_debug_status``, ``sinkattn_set_decode_kernel``,
+``sinkattn_set_prefill_kernel``.
 
 The compiled library is loaded on first use; if it has not been built, every
 call raises (there is no CPU fallback).
@@ -28,6 +29,7 @@ from ._binding import (  # noqa: F401
     sinkattn_prefill,
     sinkattn_prefill_paged,
     sinkattn_set_decode_kernel,
+    sinkattn_set_prefill_kernel,
     sinkattn_status_string,
 )
 from . import workloads  # noqa: F401

@@ -67,10 +67,12 @@ def lib() -> ctypes.CDLL:
             L.sinkattn_last_error.restype = ctypes.c_char_p
             L.sinkattn_debug_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
             L.sinkattn_set_decode_kernel.argtypes = [ctypes.c_int]
+            L.sinkattn_set_prefill_kernel.argtypes = [ctypes.c_int]
             for name in ("sinkattn_prefill", "sinkattn_decode_split", "sinkattn_merge",
                          "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc",
                          "sinkattn_decode_workspace_bytes", "sinkattn_decode_default_splits",
                          "sinkattn_debug_status", "sinkattn_set_decode_kernel",
+                         "sinkattn_set_prefill_kernel",
                          "sinkattn_prefill_paged", "sinkattn_decode_split_paged",
                          "sinkattn_decode_paged"):
                 getattr(L, name).restype = ctypes.c_int
@@ -321,6 +323,16 @@ def sinkattn_set_decode_kernel(kind) -> None:
     "tcgen05" (or the integer codes of include/sinkattn.h)."""
     code = DECODE_KERNELS[kind] if isinstance(kind, str) else int(kind)
     _check(lib().sinkattn_set_decode_kernel(code))
+
+
+PREFILL_KERNELS = {"auto": 0, "one_block": 1, "persistent": 2}
+
+
+def sinkattn_set_prefill_kernel(kind) -> None:
+    """Selects the prefill launch process-wide: "auto", "one_block" or
+    "persistent" (or the integer codes of include/sinkattn.h)."""
+    code = PREFILL_KERNELS[kind] if isinstance(kind, str) else int(kind)
+    _check(lib().sinkattn_set_prefill_kernel(code))
 
 
 def sinkattn_status_string(status: int) -> str:

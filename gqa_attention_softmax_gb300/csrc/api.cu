@@ -18,6 +18,7 @@ namespace sinkattn {
 
 static thread_local char g_last_error[512] = "";
 static std::atomic<int> g_decode_kernel{SINKATTN_DECODE_AUTO};
+static std::atomic<int> g_prefill_kernel{SINKATTN_PREFILL_AUTO};
 
 void set_error(const char* fmt, ...) {
   va_list ap;
@@ -222,7 +223,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* sinks
   set_paged(&a, pg);
   if (num_qo_heads / num_kv_heads > 128)
     return fail(SINKATTN_UNSUPPORTED, "GQA group of %d heads exceeds 128", num_qo_heads / num_kv_heads);
-  return launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
+  return launch_prefill_tc(a, g_prefill_kernel.load(std::memory_order_relaxed),
+                           static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -381,6 +383,15 @@ int sinkattn_decode_split_paged(const void* q, const void* k_pages, const void* 
   return decode_split_impl(q, k_pages, v_pages, kv_indptr, &pg, batch, q_len, max_kv_len,
                            num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window,
                            num_splits, part_acc, part_md, stream);
+}
+
+int sinkattn_set_prefill_kernel(int kind) {
+  g_last_error[0] = '\0';
+  if (kind != SINKATTN_PREFILL_AUTO && kind != SINKATTN_PREFILL_ONE_BLOCK &&
+      kind != SINKATTN_PREFILL_PERSISTENT)
+    return fail(SINKATTN_INVALID_ARG, "unknown prefill kernel %d", kind);
+  g_prefill_kernel.store(kind, std::memory_order_relaxed);
+  return SINKATTN_OK;
 }
 
 int sinkattn_set_decode_kernel(int kind) {

@@ -78,7 +78,7 @@ bool decode_tc_supported(const AttnArgs& a);
 int launch_decode_tc(const AttnArgs& a, cudaStream_t stream);
 
 // Single-pass prefill on the tcgen05/TMEM path. Returns a SINKATTN_* status.
-int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
+int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream);
 
 // drop_partials: the partials are the library's scratch (sinkattn_decode's
 // workspace): after folding a row, drop its accumulator lines from L2 without

@@ -50,6 +50,7 @@ __device__ int g_status_prefill_tc;
 struct TcParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
+  int batch, n_items;
   int Hq, Hkv, G, QB, nqb, max_kv;
   float sm_scale, scale_log2;
   int causal, window;
@@ -79,8 +80,11 @@ struct TcCfg {
   static constexpr int STAGE = 2 * KV_TILE;       // K and V of one KV tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
-  static constexpr int OFF_BAR = OFF_KV + NST * STAGE;
-  static constexpr int N_BARS = 1 + 2 * NST + NSB + 2 + 2 + 1;
+  static constexpr int LIST_CAP = 512;            // items per CTA in the snake list
+  static constexpr int CUQ_CAP = 1025;            // sequences staged for the item scan
+  static constexpr int OFF_LIST = OFF_KV + NST * STAGE;   // [LIST_CAP + 32 + CUQ_CAP] ints
+  static constexpr int OFF_BAR = OFF_LIST + ((LIST_CAP + 32 + CUQ_CAP) * 4 + 15) / 16 * 16;
+  static constexpr int N_BARS = 2 + 2 * NST + NSB + 2 + 2 + NSB + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
   static constexpr int THREADS = 320;             // TMA, MMA, 2 tiles x 4 softmax warps
   static constexpr uint32_t TMEM_COLS = 512;
@@ -97,6 +101,9 @@ struct TcCfg {
   static_assert(KVSUB % 1024 == 0 && KT % 32 == 0, "tile shape");
 };
 
+// One block per item: block (x, y, z) runs query block nqb - 1 - x of KV head
+// y of sequence z (longest query blocks launch first), the hardware deals the
+// blocks out to the SMs as they free up.
 template <int D, int NST>
 __global__ void __launch_bounds__(320, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -528,9 +535,577 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// One work item: both query tiles of (sequence b, KV head kvh, query block qb)
+// and the KV tiles they visit. n < 0: the block has no query rows; n == 0:
+// rows but no visible key (the epilogue alone runs).
+struct PfItem {
+  int b, kvh, q_start, Lq, q0, nq, k_start, Lk, pos0, k_lo, k_hi, n, first;
+};
+
+template <int KT>
+__device__ __forceinline__ PfItem pf_item(const TcParams& p, int it) {
+  PfItem t;
+  const int per = p.Hkv * p.batch;
+  const int qb = p.nqb - 1 - it / per;   // longest query blocks first
+  const int r = it % per;
+  t.kvh = r % p.Hkv;
+  t.b = r / p.Hkv;
+  t.q_start = p.cu_q[t.b];
+  t.Lq = p.cu_q[t.b + 1] - t.q_start;
+  t.k_start = p.cu_k[t.b];
+  t.Lk = p.cu_k[t.b + 1] - t.k_start;
+  t.q0 = qb * 2 * p.QB;   // first token of tile A
+  t.nq = 0;
+  t.pos0 = t.k_lo = t.k_hi = t.first = 0;
+  t.n = -1;
+  if (t.q0 >= t.Lq) return t;
+  t.nq = min(2 * p.QB, t.Lq - t.q0);
+  t.pos0 = t.Lk - t.Lq + t.q0;
+  const int posN = t.pos0 + t.nq - 1;
+  t.k_hi = t.Lk;
+  if (p.causal) t.k_hi = min(t.k_hi, posN + 1);
+  if (p.window > 0) t.k_lo = max(0, t.pos0 - p.window + 1);
+  // Tiles end at k_hi (contiguous: no copy reads past the last key needed),
+  // or start on a multiple of KT (paged: no box straddles a page).
+  const bool paged = p.page_size > 0;
+  const int t0 = t.k_lo / KT * KT;
+  t.n = (t.k_hi > t.k_lo) ? (t.k_hi - (paged ? t0 : t.k_lo) + KT - 1) / KT : 0;
+  t.first = paged ? t0 : t.k_hi - t.n * KT;
+  return t;
+}
+
+// Persistent: CTA c runs items c, c + gridDim.x, ... (one CTA per SM, TMEM
+// allocated once). KV tiles, S buffers and every barrier phase are counted
+// across items, so the K/V ring streams on from one item into the next; the
+// next item's Q is loaded as soon as the tensor core has finished the
+// current item's last S.
+template <int D, int NST>
+__global__ void __launch_bounds__(320, 1)
+    prefill_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  using C = TcCfg<D, NST>;
+  constexpr int KT = C::KT;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;             // Q of the item landed (by active item ordinal)
+  uint64_t* q_empty = q_full + 1;      // the item's last S completed: Q may be replaced
+  uint64_t* kv_full = q_empty + 1;
+  uint64_t* kv_empty = kv_full + NST;
+  uint64_t* s_full = kv_empty + NST;   // [NSB]: S written into buffer b
+  uint64_t* p_full = s_full + C::NSB;  // [2]: P_t written and O_t rescaled (128 arrivals)
+  uint64_t* pv_done = p_full + 2;      // [2]: PV_t completed (one buffer per tile)
+  uint64_t* pv_buf = pv_done + 2;      // [NSB]: the P.V reading buffer b completed (ring)
+  uint64_t* drain = pv_buf + C::NSB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* status = &g_status_prefill_tc;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int* list = reinterpret_cast<int*>(smem + C::OFF_LIST);      // [LIST_CAP] this CTA's items
+  int* scan = list + C::LIST_CAP;                               // [16] per-warp counts, [16] misc
+  int* cuq_s = scan + 32;                                       // [CUQ_CAP] staged cu_seqlens_q
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < C::NSB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&pv_buf[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&p_full[t], 128);
+      mbar_init(&pv_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+
+  // This CTA's items. Items (the rectangle of query blocks x KV heads x
+  // sequences, longest query blocks first) that have query rows are ranked in
+  // that order and dealt out in snake order -- rank r of round r / G goes to
+  // CTA r % G on even rounds and G - 1 - r % G on odd ones -- so every CTA
+  // gets one item of each round and the loads differ by about one small
+  // item. Without room for the list, items go round-robin.
+  const int G = static_cast<int>(gridDim.x);
+  const bool staged = p.batch + 1 <= C::CUQ_CAP;
+  if (staged)
+    for (int i = threadIdx.x; i <= p.batch; i += blockDim.x) cuq_s[i] = p.cu_q[i];
+  __syncthreads();
+  const int per = p.Hkv * p.batch;
+  auto has_rows = [&](int it) -> bool {
+    const int qb = p.nqb - 1 - it / per;
+    const int b = (it % per) / p.Hkv;
+    const int Lq = staged ? cuq_s[b + 1] - cuq_s[b] : p.cu_q[b + 1] - p.cu_q[b];
+    return qb * 2 * p.QB < Lq;
+  };
+  int n_list = 0, total = 0;
+  bool use_list = staged;
+  if (use_list) {
+    const int nw = blockDim.x >> 5;
+    for (int base = 0; base < p.n_items; base += blockDim.x) {
+      const int it = base + static_cast<int>(threadIdx.x);
+      const bool f = it < p.n_items && has_rows(it);
+      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      if (lane == 0) scan[warp] = __popc(bal);
+      __syncthreads();
+      int before = total;
+      for (int w = 0; w < warp; ++w) before += scan[w];
+      int chunk = 0;
+      for (int w = 0; w < nw; ++w) chunk += scan[w];
+      if (f) {
+        const int r = before + __popc(bal & ((1u << lane) - 1u));
+        const int round = r / G, pos = r - round * G;
+        const int cta = (round & 1) ? G - 1 - pos : pos;
+        if (cta == static_cast<int>(blockIdx.x) && round < C::LIST_CAP) list[round] = it;
+      }
+      total += chunk;
+      __syncthreads();
+    }
+    const int rounds = (total + G - 1) / G;
+    if (rounds > C::LIST_CAP) {
+      use_list = false;
+    } else {
+      // rounds in which this CTA got an item: all but possibly the last
+      const int last = rounds - 1;
+      const int last_n = total - last * G;   // items of the last round
+      const int pos_last = (last & 1) ? G - 1 - static_cast<int>(blockIdx.x)
+                                      : static_cast<int>(blockIdx.x);
+      n_list = (rounds > 0 && pos_last >= last_n) ? last : rounds;
+    }
+  }
+  const int n_mine = use_list ? n_list
+                              : (p.n_items - static_cast<int>(blockIdx.x) + G - 1) / G;
+  auto item_of = [&](int k) -> int {
+    return use_list ? list[k] : static_cast<int>(blockIdx.x) + k * G;
+  };
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    // The warp runs the loop (page lists are read 32 entries per warp load);
+    // lane 0 issues every other copy.
+    const bool leader = (lane == 0);
+    auto pwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+    };
+    if (leader) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
+    const uint32_t q_bytes = static_cast<uint32_t>(2 * C::NSUB * 128 * p.G * p.QB);
+    int g = 0, qi = 0;   // KV tiles and active items so far
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const PfItem t = pf_item<KT>(p, item_of(k));
+      if (t.n < 0) continue;
+      if (leader && (t.Lk < t.Lq || t.Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
+      if (t.n == 0) continue;
+      if (qi > 0 && !pwait(q_empty, (qi - 1) & 1)) { ok = false; break; }
+      if (leader) {
+        mbar_arrive_expect_tx(q_full, q_bytes);
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+          for (int sub = 0; sub < C::NSUB; ++sub)
+            tc::tma_load_3d(smem + C::OFF_Q + tt * C::Q_TILE + sub * C::QSUB, &tmQ, sub * 64,
+                            t.kvh * p.G, t.q_start + t.q0 + tt * p.QB, q_full);
+      }
+      ++qi;
+      const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // contiguous: tensor-map row of key 0
+      PageCursor pc;
+      if (p.page_size > 0) {
+        const int e0 = p.page_indptr[t.b];
+        const int np = p.page_indptr[t.b + 1] - e0;
+        if (leader && t.Lk > np * p.page_size) atomicExch(status, SINKATTN_BAD_LENGTHS);
+        pc.start(p.page_indices + e0, np, t.first / p.page_size, lane);
+      }
+      for (int i = 0; i < t.n; ++i, ++g) {
+        const int st = g % NST;
+        if (!pwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
+        uint8_t* kt = smem + C::OFF_KV + st * C::STAGE;
+        if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+        const int j0 = t.first + i * KT;
+        if (p.page_size == 0) {
+          if (leader) {
+#pragma unroll
+            for (int sub = 0; sub < C::NSUB; ++sub) {
+              tma_load_2d_hint(kt + sub * C::KVSUB, &tmK, sub * 64, slab + j0, &kv_full[st],
+                               policy);
+              tma_load_2d_hint(kt + C::KV_TILE + sub * C::KVSUB, &tmV, sub * 64, slab + j0,
+                               &kv_full[st], policy);
+            }
+          }
+        } else {
+          // one box per page segment, lane i issuing box i: rows (page,
+          // head, slot) of the pool
+          const int nbox = KT / p.box_rows;
+          const int a = j0 + min(lane, nbox - 1) * p.box_rows;
+          const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
+          if (lane < nbox) {
+            const int row = (page * p.Hkv + t.kvh) * p.page_size + a % p.page_size;
+            const int off = (a - j0) * 128;
+#pragma unroll
+            for (int sub = 0; sub < C::NSUB; ++sub) {
+              tma_load_2d_hint(kt + sub * C::KVSUB + off, &tmK, sub * 64, row, &kv_full[st],
+                               policy);
+              tma_load_2d_hint(kt + C::KV_TILE + sub * C::KVSUB + off, &tmV, sub * 64, row,
+                               &kv_full[st], policy);
+            }
+          }
+        }
+      }
+    }
+    if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
+      if (qi > 0) mbar_drain(q_full, (qi - 1) & 1);
+      for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    // The whole warp runs the schedule (waits and descriptor arithmetic stay
+    // warp-uniform); one elected lane issues each MMA and commit.
+    const bool leader = tc::elect_one();
+    auto wwait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+    };
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, C::NO, true);
+    constexpr uint64_t STAGE16 = C::STAGE >> 4;   // one K/V stage, in descriptor address units
+    constexpr uint64_t QSUB16 = C::QSUB >> 4;
+    constexpr uint64_t KVSUB16 = C::KVSUB >> 4;
+    // Descriptors prepared once: a K step (16 elements = 32 bytes) within a
+    // 128-byte swizzle row adds 2 to the address field, the next 64-column
+    // block adds its size / 16, a stage adds STAGE / 16, 16 keys of V add 128.
+    const uint64_t qd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+    const uint64_t kd0 = tc::smem_desc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+    // V is MN-major: its 64-column blocks are KVSUB bytes apart.
+    const uint32_t v_base0 = smem_u32(smem + C::OFF_KV + C::KV_TILE);
+    const uint64_t vd0 = tc::smem_desc_sw128(v_base0, static_cast<uint32_t>(C::KVSUB), 1024);
+    // S_t of global KV tile g
+    auto issue_s = [&](int t, int g) {
+      const int buf = C::buf_of(t, g);
+      const uint64_t kd = kd0 + static_cast<uint64_t>(g % NST) * STAGE16;
+      const uint64_t qd = qd0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
+      const uint32_t d_tm = tmem + C::col_s(buf);
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t step = static_cast<uint64_t>(kk & 3) * 2;
+          tc::mma_ss(d_tm, qd + static_cast<uint64_t>(kk >> 2) * QSUB16 + step,
+                     kd + static_cast<uint64_t>(kk >> 2) * KVSUB16 + step, idesc_s,
+                     kk > 0 ? 1u : 0u);
+        }
+        tc::commit(&s_full[buf]);
+      }
+      __syncwarp();
+    };
+    // PV_t of global KV tile g; the item's first PV overwrites O_t
+    auto issue_pv = [&](int t, int g, bool first_of_item) {
+      const uint64_t vd = vd0 + static_cast<uint64_t>(g % NST) * STAGE16;
+      const uint32_t d_tm = tmem + C::col_o(t);
+      const uint32_t a_tm = tmem + C::col_s(C::buf_of(t, g));
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk)
+          tc::mma_ts(d_tm, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u, idesc_o,
+                     (!first_of_item || kk > 0) ? 1u : 0u);
+        // ring: one barrier per S buffer (the buffer's next S waits for it);
+        // one buffer per tile: one barrier per tile
+        tc::commit(C::RING ? &pv_buf[C::buf_of(t, g)] : &pv_done[t]);
+      }
+      __syncwarp();
+    };
+    auto commit1 = [&](uint64_t* bar) {
+      if (leader) tc::commit(bar);
+      __syncwarp();
+    };
+    int g = 0, qi = 0;   // KV tiles and active items so far
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const PfItem t = pf_item<KT>(p, item_of(k));
+      if (t.n <= 0) continue;
+      if (!wwait1(q_full, qi & 1)) { ok = false; break; }
+      const int g0 = g, n = t.n;
+      if constexpr (C::RING) {
+        // Steps ranked k = 2 g + t (tile t at global KV tile g). S(k0 .. k0+2)
+        // of the item, then per step PV(k) and S(k + 3), the latter into the
+        // buffer of PV(k - 1) once that has completed; PV(k) is queued
+        // meanwhile, so the tensor core does not drain at the hand-off.
+        const int k0 = 2 * g0, kend = 2 * (g0 + n);
+        auto s_step = [&](int k) -> bool {
+          const int gt = k >> 1, tt = k & 1;
+          if (tt == 0 && !wwait1(&kv_full[gt % NST], (gt / NST) & 1)) return false;
+          if (k >= C::NSB && !wwait1(&pv_buf[k % C::NSB], ((k - C::NSB) / C::NSB) & 1))
+            return false;
+          tc::fence_after_sync();
+          issue_s(tt, gt);
+          if (k == kend - 1) commit1(q_empty);   // the item's last S: Q may be replaced
+          return true;
+        };
+        for (int k = k0; ok && k < min(k0 + 3, kend); ++k) ok = s_step(k);
+        for (int k = k0; ok && k < kend; ++k) {
+          const int gt = k >> 1, tt = k & 1;
+          if (!wwait1(&p_full[tt], gt & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          issue_pv(tt, gt, gt == g0);
+          if (tt == 1) commit1(&kv_empty[gt % NST]);
+          if (k + 3 < kend) ok = s_step(k + 3);
+        }
+      } else {
+        // One buffer per tile: S_A(g0) S_B(g0), then per KV tile g and tile
+        // t: PV_t(g), then S_t(g+1) into the same buffer once PV_t(g) is done.
+        for (int tt = 0; ok && tt < 2; ++tt) {
+          if (tt == 0 && !wwait1(&kv_full[g0 % NST], (g0 / NST) & 1)) { ok = false; break; }
+          if (g0 > 0 && !wwait1(&pv_done[tt], (g0 - 1) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          issue_s(tt, g0);
+          if (n == 1 && tt == 1) commit1(q_empty);
+        }
+        for (int jj = 0; ok && jj < n; ++jj) {
+          const int gg = g0 + jj;
+          for (int tt = 0; tt < 2; ++tt) {
+            if (!wwait1(&p_full[tt], gg & 1)) { ok = false; break; }
+            tc::fence_after_sync();
+            issue_pv(tt, gg, jj == 0);
+            if (tt == 1) commit1(&kv_empty[gg % NST]);
+            if (jj + 1 < n) {
+              if (tt == 0 && !wwait1(&kv_full[(gg + 1) % NST], ((gg + 1) / NST) & 1)) { ok = false; break; }
+              if (!wwait1(&pv_done[tt], gg & 1)) { ok = false; break; }
+              tc::fence_after_sync();
+              issue_s(tt, gg + 1);
+              if (jj + 2 == n && tt == 1) commit1(q_empty);
+            }
+          }
+        }
+      }
+      g += n;
+      ++qi;
+    }
+    // every MMA this warp issued has completed before the CTA frees TMEM
+    commit1(drain);
+    mbar_drain(drain, 0);
+  } else {
+    // ---------------------------------------------------------------- softmax
+    // 8 warps: tile t = A/B; warp w may access TMEM lanes 32 (w % 4) ...
+    const int t = (warp - 2) >> 2;
+    const int quad = warp & 3;       // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;
+    const int G = p.G;
+    const int rg = row / G;          // token within the tile
+    const int hig = row - rg * G;    // head within the group
+    const float c2 = p.scale_log2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t o_addr = lane_base + C::col_o(t);
+    constexpr int NCH = KT / 32;     // 32-column chunks of a score row
+    // A wait that gives up in any lane makes the whole warp leave, so the
+    // warp-collective TMEM loads/stores below never run with missing lanes.
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+    };
+    // wait for PV_t of global KV tile gg
+    auto pv_wait = [&](int gg) -> bool {
+      return C::RING ? wwait(&pv_buf[C::buf_of(t, gg)], C::use_of(t, gg) & 1)
+                     : wwait(&pv_done[t], gg & 1);
+    };
+    int g = 0;   // KV tiles so far
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const PfItem it_ = pf_item<KT>(p, item_of(k));
+      if (it_.n < 0) continue;
+      const int n = it_.n;
+      const int tl = t * p.QB + rg;    // token within the item
+      const bool valid = rg < p.QB && tl < it_.nq;
+      const int pos = it_.pos0 + tl;
+      const int h = it_.kvh * G + hig;
+      const int tok = it_.q_start + it_.q0 + tl;
+      int lo_r = it_.k_lo, hi_r = it_.k_hi - 1;
+      if (p.window > 0) lo_r = max(lo_r, pos - p.window + 1);
+      if (p.causal) hi_r = min(hi_r, pos);
+
+      // l: the row's running sum, the sink's term included (for out and
+      // lse). The running maximum is exact, so the row's largest weight is
+      // exactly 1 and the P.V MMA's bf16 rounding of the others stays below
+      // 2^-8 of each.
+      float m_used = kNegInf, l = 0.f;
+      if (p.sinks != nullptr && valid) {
+        const float s = p.sinks[h];
+        if (s != kNegInf) {
+          m_used = s / p.sm_scale;   // the sink, in raw logit units
+          l = 1.f;
+        }
+      }
+
+      for (int j = 0; j < n; ++j) {
+        const int gg = g + j;
+        const int buf = C::buf_of(t, gg);
+        if (!wwait(&s_full[buf], C::use_of(t, gg) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t s_addr = lane_base + C::col_s(buf);
+        const int j0 = it_.first + j * KT;
+        const bool masked = (j0 < lo_r || j0 + KT - 1 > hi_r);
+        const int clo = lo_r - j0, chi = hi_r - j0;
+
+        // the row's KT scores, one batch of loads
+        float v[NCH][32];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) tc::tmem_ld32(s_addr + 32 * c, v[c]);
+        tc::tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const int lo_c = clo - c * 32, hi_c = chi - c * 32;
+            if (lo_c <= 0 && hi_c >= 31) continue;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (e < lo_c || e > hi_c) v[c][e] = kNegInf;
+          }
+        }
+        // row maximum: 2 NCH independent chains of three-input maxima
+        float mxc[2 * NCH];
+#pragma unroll
+        for (int i = 0; i < 2 * NCH; ++i)
+          mxc[i] = fmaxf(v[i >> 1][(i & 1) * 16], v[i >> 1][(i & 1) * 16 + 1]);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int e = 2; e < 16; e += 2) {
+            mxc[2 * c] = fmax3(mxc[2 * c], v[c][e], v[c][e + 1]);
+            mxc[2 * c + 1] = fmax3(mxc[2 * c + 1], v[c][16 + e], v[c][16 + e + 1]);
+          }
+        float mx = fmax3(mxc[0], mxc[1], mxc[2]);
+#pragma unroll
+        for (int i = 3; i < 2 * NCH; i += 2)
+          mx = (i + 1 < 2 * NCH) ? fmax3(mx, mxc[i], mxc[i + 1]) : fmaxf(mx, mxc[i]);
+
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_used) {
+          alpha = (m_used == kNegInf) ? 0.f : ex2((m_used - mx) * c2);
+          m_used = mx;
+          rescale = true;
+        }
+        const float mb = (m_used == kNegInf) ? 0.f : m_used * c2;
+
+        // P = 2^(s*c2 - mb) as bf16 into the first KT / 2 columns of this S
+        // buffer (all KT scores are already in registers). Scale-subtract and
+        // the exact sum run two lanes per instruction (paired fp32 FMA / add).
+        const float2 c2x2 = make_float2(c2, c2), nmb2 = make_float2(-mb, -mb);
+        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int k = hh * 16 + e;
+              const float2 x = __ffma2_rn(make_float2(v[c][k], v[c][k + 1]), c2x2, nmb2);
+              const float2 a = make_float2(ex2(x.x), ex2(x.y));
+              rs2[(e >> 1) & 3] = __fadd2_rn(rs2[(e >> 1) & 3], a);
+              pk[e >> 1] = pack_bf16x2(a.x, a.y);
+            }
+            tc::tmem_st8(s_addr + 16 * c + 8 * hh, pk);
+          }
+        const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+        const float rs = rsa.x + rsa.y;
+
+        // Two buffers per tile: PV_t(j-1) has completed before O_t is touched
+        // or P_t(j) is handed over (so p_full[t] cannot run two phases ahead
+        // of the MMA warp). With one buffer S_t(j) was issued after PV_t(j-1);
+        // at j = 0 the previous item's epilogue waited for its last PV_t.
+        if (C::RING && j >= 1) {
+          if (!pv_wait(gg - 1)) { ok = false; break; }
+          tc::fence_after_sync();
+        }
+        // Rescale the row's O_t when some row of this warp moved its maximum
+        // (warp-uniform branch).
+        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc::tmem_ld32(o_addr + c * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tc::tmem_st32(o_addr + c * 32, o);
+          }
+        }
+        tc::tmem_wait_st();
+        l = l * alpha + rs;
+        tc::fence_before_sync();
+        mbar_arrive(&p_full[t]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      // O_t is read out before this thread hands P of the next item over,
+      // so the next item's first PV (which overwrites O_t) comes after it.
+      if (n >= 1) {
+        if (!pv_wait(g + n - 1)) { ok = false; break; }
+        tc::fence_after_sync();
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (n >= 1) {
+          tc::tmem_ld32(o_addr + c * 32, o);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 pk;
+            pk.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+            pk.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+            pk.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+            pk.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = pk;
+          }
+        }
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[static_cast<size_t>(tok) * p.Hq + h] =
+            l > 0.f ? (m_used * c2 + lg2(l)) * kLn2 : kNegInf;
+      g += n;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------------------
 template <int D, int NST>
-static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
+static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   using C = TcCfg<D, NST>;
   const int G = a.Hq / a.Hkv;
   CUtensorMap tmQ, tmK, tmV;
@@ -556,6 +1131,13 @@ static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
   p.G = G;
   p.QB = QB;
   p.nqb = (a.max_q + 2 * QB - 1) / (2 * QB);
+  p.batch = a.batch;
+  const int64_t items = static_cast<int64_t>(p.nqb) * a.Hkv * a.batch;
+  if (items >= (int64_t{1} << 31)) {
+    set_error("too many prefill work items");
+    return SINKATTN_UNSUPPORTED;
+  }
+  p.n_items = static_cast<int>(items);
   p.max_kv = a.max_kv;
   p.sm_scale = a.sm_scale;
   p.scale_log2 = a.sm_scale * kLog2e;
@@ -565,14 +1147,16 @@ static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
 
-  auto kern = prefill_tc_kernel<D, NST>;
+  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST> : prefill_tc_kernel<D, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     return SINKATTN_CUDA_ERROR;
   }
-  const dim3 grid(static_cast<unsigned>(p.nqb), static_cast<unsigned>(a.Hkv),
-                  static_cast<unsigned>(a.batch));
+  if (p.n_items == 0) return SINKATTN_OK;
+  const dim3 grid = persistent ? dim3(static_cast<unsigned>(std::min<int64_t>(items, sm_count())))
+                               : dim3(static_cast<unsigned>(p.nqb), static_cast<unsigned>(a.Hkv),
+                                      static_cast<unsigned>(a.batch));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmQ, tmK, tmV, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -582,14 +1166,33 @@ static int launch_tc(const AttnArgs& a, cudaStream_t stream) {
   return SINKATTN_OK;
 }
 
-int launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
+// Persistent CTAs pay off when items are short (a few KV tiles: a sliding
+// window, short prompts), where the one-block-per-item launch spends much of
+// its time starting and finishing blocks; with long items the one-block
+// launch measured faster (full-causal gpt-oss-shaped prefill 737 against
+// 680 TFLOP/s).
+static bool prefer_persistent(const AttnArgs& a, int kt) {
+  const int G = a.Hq / a.Hkv;
+  const int tokens = 2 * (128 / G);   // query tokens per item
+  const long long keys = a.window > 0 ? static_cast<long long>(a.window) + tokens
+                                      : (a.causal ? a.max_kv / 2 : a.max_kv);
+  return keys <= 6LL * kt;
+}
+
+int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   if (G > 128) {
     set_error("GQA group of %d query heads exceeds the 128 rows of a tile", G);
     return SINKATTN_UNSUPPORTED;
   }
-  if (a.d == 64) return launch_tc<64, 4>(a, stream);
-  return launch_tc<128, 2>(a, stream);
+  if (a.d == 64) {
+    const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
+                      (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<64, 4>::KT));
+    return launch_tc<64, 4>(a, pers, stream);
+  }
+  const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
+                    (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<128, 2>::KT));
+  return launch_tc<128, 2>(a, pers, stream);
 }
 
 int read_status_prefill_tc(cudaStream_t s, int* status) {

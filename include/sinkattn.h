@@ -232,6 +232,23 @@ SINKATTN_API int sinkattn_decode_default_splits(int32_t batch, int32_t q_len, in
 SINKATTN_API int sinkattn_set_decode_kernel(int kind);
 
 /*
+ * Process-wide choice of the prefill launch (both run the same tcgen05
+ * kernel body and give the same results up to floating-point rounding order):
+ *   SINKATTN_PREFILL_AUTO (0, default): persistent when the work items are
+ *     short (a sliding window, or prompts of a few KV tiles), else one block
+ *     per item;
+ *   SINKATTN_PREFILL_ONE_BLOCK (1): one thread block per (query block, KV
+ *     head, sequence), scheduled by the hardware;
+ *   SINKATTN_PREFILL_PERSISTENT (2): one thread block per SM working through
+ *     a fixed list of items, streaming K/V across item boundaries.
+ * Returns SINKATTN_INVALID_ARG for any other value.
+ */
+#define SINKATTN_PREFILL_AUTO 0
+#define SINKATTN_PREFILL_ONE_BLOCK 1
+#define SINKATTN_PREFILL_PERSISTENT 2
+SINKATTN_API int sinkattn_set_prefill_kernel(int kind);
+
+/*
  * Paged KV cache (HND within a page: heads leading, tokens contiguous): the
  * same operations as sinkattn_prefill, sinkattn_decode_split and
  * sinkattn_decode, with K and V held in page pools

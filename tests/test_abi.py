@@ -202,3 +202,10 @@ def test_decode_paged_checks_workspace_before_launch(L):
     rc = L.sinkattn_decode_paged(A, B, C, 0x5000, 0x9000, 0xA000, 8, 16, 2, 1, 100, 8, 1, 128, 0.1,
                                  1, 0, 4, None, 0x10000, need, O, None, None)
     assert rc != 1 or "workspace" not in sa.sinkattn_last_error()
+
+
+def test_prefill_kernel_switch(L):
+    assert L.sinkattn_set_prefill_kernel(3) == 1
+    assert L.sinkattn_set_prefill_kernel(-1) == 1
+    for k in (1, 2, 0):
+        assert L.sinkattn_set_prefill_kernel(k) == 0

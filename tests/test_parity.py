@@ -71,15 +71,59 @@ PREFILL_CASES = [
 
 @pytest.mark.parametrize("case", PREFILL_CASES, ids=lambda c: "q%s_k%s_h%d-%d_d%d_c%d_w%d_%s_x%g" % (
     "-".join(map(str, c[0])), "-".join(map(str, c[1])), c[2], c[3], c[4], c[5], c[6], c[7], c[8]))
-def test_prefill_matches_oracle(case):
+@pytest.mark.parametrize("launch", ["one_block", "persistent"])
+def test_prefill_matches_oracle(case, launch):
     q_lens, kv_lens, Hq, Hkv, d, causal, window, sk, qs = case
     inp = workloads.explicit_inputs(q_lens, kv_lens, Hq, Hkv, d, seed=21, q_scale=qs)
     sinks = _sinks(sk, Hq, inp["sinks"])
     scale = 1.0 / math.sqrt(d)
     want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], sinks, inp["cu_q"],
                                        inp["cu_k"], Hq, Hkv, d, scale, causal, window)
-    out, lse = _run_prefill(inp, Hq, Hkv, d, scale, causal, window, sinks)
-    compare(out, lse, want_out, want_lse, "prefill")
+    sa.sinkattn_set_prefill_kernel(launch)
+    try:
+        out, lse = _run_prefill(inp, Hq, Hkv, d, scale, causal, window, sinks)
+    finally:
+        sa.sinkattn_set_prefill_kernel("auto")
+    compare(out, lse, want_out, want_lse, "prefill " + launch)
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,window,page", [(64, 16, 8, 0, 0), (128, 16, 4, 0, 0),
+                                                  (64, 8, 2, 40, 0), (64, 16, 8, 0, 32),
+                                                  (128, 8, 8, 0, 16)])
+@pytest.mark.parametrize("launch", ["one_block", "persistent"])
+def test_prefill_many_items_per_cta(d, Hq, Hkv, window, page, launch):
+    """More (query block, KV head, sequence) items than SMs, so every CTA of
+    the persistent prefill runs several items back to back (the K/V ring, S
+    buffers and barrier phases carry over); varied lengths, some sequences
+    with fewer queries than keys and some with none."""
+    sa.sinkattn_set_prefill_kernel(launch)
+    try:
+        _many_items(d, Hq, Hkv, window, page)
+    finally:
+        sa.sinkattn_set_prefill_kernel("auto")
+
+
+def _many_items(d, Hq, Hkv, window, page):
+    rng = np.random.default_rng(17 + d + window + page)
+    B = 64
+    kv_lens = rng.integers(1, 320, size=B).tolist()
+    q_lens = [int(min(k, max(0, rng.integers(-20, k + 1)))) for k in kv_lens]
+    inp = workloads.explicit_inputs(q_lens, kv_lens, Hq, Hkv, d, seed=29)
+    scale = 1.0 / math.sqrt(d)
+    want_out, want_lse = oracle.attend(inp["q"], inp["k"], inp["v"], inp["sinks"], inp["cu_q"],
+                                       inp["cu_k"], Hq, Hkv, d, scale, True, window)
+    g = to_dev(inp)
+    if page:
+        pg = to_dev(workloads.to_paged(inp, Hkv, page, seed=3))
+        out, lse = sa.sinkattn_prefill_paged(g["q"], pg["k_pages"], pg["v_pages"], g["sinks"],
+                                             g["cu_q"], g["cu_k"], pg["page_indptr"],
+                                             pg["page_indices"], max(q_lens), max(kv_lens),
+                                             scale, True, window)
+    else:
+        out, lse = sa.sinkattn_prefill(g["q"], g["k"], g["v"], g["sinks"], g["cu_q"], g["cu_k"],
+                                       max(q_lens), max(kv_lens), Hkv, scale, True, window)
+    torch.cuda.synchronize()
+    compare(out, lse, want_out, want_lse, "prefill, many items per CTA")
 
 
 def test_tiny_workload_prefill_and_decode():
