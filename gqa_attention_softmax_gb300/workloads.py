@@ -215,3 +215,28 @@ def to_paged(inp: dict, Hkv: int, page_size: int, seed: int = 0, spare_pages: in
     vp.view(-1, d)[dest] = v
     return dict(k_pages=kp, v_pages=vp, page_indptr=indptr.to(torch.int32).to(dev),
                 page_indices=perm[:used].to(torch.int32).to(dev))
+
+
+def to_fp8(inp: dict, Hkv: int) -> dict:
+    """An FP8 (e4m3) copy of the ragged HND ``k``/``v`` of ``inp``: per KV head
+    g, scale[g] = max |x| over that head's keys (or values) / 448 (the largest
+    e4m3 magnitude), codes = x / scale[g] rounded to nearest even e4m3 (torch's
+    float8_e4m3fn conversion), stored as uint8. Returns k_fp8, v_fp8 (uint8,
+    same layout) and k_scale, v_scale (fp32 [Hkv]) on the device of
+    ``inp["k"]``. Pure data preparation."""
+    out = {}
+    cu = inp["cu_k"].cpu().tolist()
+    for name in ("k", "v"):
+        x = inp[name].float()
+        heads = torch.zeros_like(x[:, 0], dtype=torch.int64)
+        for b in range(len(cu) - 1):
+            L = cu[b + 1] - cu[b]
+            r0 = Hkv * cu[b]
+            heads[r0:r0 + Hkv * L] = torch.arange(Hkv, device=x.device).repeat_interleave(L)
+        amax = torch.zeros(Hkv, dtype=torch.float32, device=x.device)
+        amax = amax.scatter_reduce(0, heads, x.abs().amax(dim=1), reduce="amax")
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        codes = (x / scale[heads][:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        out[name + "_fp8"] = codes
+        out[name + "_scale"] = scale
+    return out

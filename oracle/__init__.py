@@ -8,6 +8,9 @@ arithmetic.
 
 Two independent implementations live here:
 
+* ``attend`` / ``split_partials`` also take K/V as e4m3 codes (uint8) with
+  per-KV-head scales (the FP8 KV cache), decoded from the E4M3 format's
+  definition (``e4m3_table`` exposes the decode);
 * ``attend`` / ``split_partials`` / ``chunk_partial`` / ``merge``: a C++
   float64 library (``sinkattn_oracle.cpp``, OpenMP over rows) that
   materialises every visible logit row plus the sink column, following
@@ -70,8 +73,15 @@ def _load():
             lib.oracle_chunk_partial.argtypes = [P, P, P, P, P, I, I, I, I, D, I, I, I64, I64, I64, P, P, P]
             lib.oracle_merge.argtypes = [P, P, P, P, I64, I, I, I, P, P]
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_attend_rows_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, D, I, I, I64,
+                                                   P, P, P]
+            lib.oracle_split_partials_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, D, I, I, I,
+                                                      P, P, P]
+            lib.oracle_e4m3_table.argtypes = [P]
             for f in (lib.oracle_attend_rows, lib.oracle_split_partials,
-                      lib.oracle_chunk_partial, lib.oracle_merge, lib.oracle_num_threads):
+                      lib.oracle_chunk_partial, lib.oracle_merge, lib.oracle_num_threads,
+                      lib.oracle_attend_rows_fp8, lib.oracle_split_partials_fp8,
+                      lib.oracle_e4m3_table):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -89,6 +99,23 @@ def _bits(x) -> np.ndarray:
     import torch
     assert x.dtype == torch.bfloat16, x.dtype
     return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _codes(x) -> np.ndarray:
+    """uint8 tensor / array of e4m3 codes -> contiguous uint8 numpy array."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint8
+        return np.ascontiguousarray(x)
+    import torch
+    assert x.dtype == torch.uint8, x.dtype
+    return np.ascontiguousarray(x.detach().cpu().contiguous().numpy())
+
+
+def _is_codes(x) -> bool:
+    if isinstance(x, np.ndarray):
+        return x.dtype == np.uint8
+    import torch
+    return x.dtype == torch.uint8
 
 
 def _f64(x) -> np.ndarray | None:
@@ -109,18 +136,28 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def e4m3_table() -> np.ndarray:
+    """Value of each of the 256 e4m3 codes (NaN codes: NaN), float64."""
+    out = np.zeros(256, dtype=np.float64)
+    _load().oracle_e4m3_table(_ptr(out))
+    return out
+
+
 def attend(q, k, v, sinks, cu_q, cu_k, num_qo_heads, num_kv_heads, head_dim,
-           sm_scale, causal, window=0, rows=None):
+           sm_scale, causal, window=0, rows=None, k_scale=None, v_scale=None):
     """Full-row float64 attention with sink.
 
     q: bf16 [total_q, Hq, d]; k, v: bf16 ragged HND (sequence b is a contiguous
-    [Hkv, Lk_b, d] block starting at element Hkv*cu_k[b]*d); sinks: [Hq] or
-    None; cu_q, cu_k: int [B+1]. rows: optional array of flat row ids
-    (token * Hq + head). Returns (out [n, d] float64, lse [n] float64), with
-    n = len(rows) or total_q * Hq.
+    [Hkv, Lk_b, d] block starting at element Hkv*cu_k[b]*d), or uint8 e4m3
+    codes in that layout with per-KV-head scales k_scale, v_scale [Hkv];
+    sinks: [Hq] or None; cu_q, cu_k: int [B+1]. rows: optional array of flat
+    row ids (token * Hq + head). Returns (out [n, d] float64, lse [n]
+    float64), with n = len(rows) or total_q * Hq.
     """
     lib = _load()
-    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    fp8 = _is_codes(k)
+    qb = _bits(q)
+    kb, vb = (_codes(k), _codes(v)) if fp8 else (_bits(k), _bits(v))
     s = _f64(sinks)
     cq, ck = _i32(cu_q), _i32(cu_k)
     B = len(cq) - 1
@@ -132,16 +169,24 @@ def attend(q, k, v, sinks, cu_q, cu_k, num_qo_heads, num_kv_heads, head_dim,
         n = len(r)
     out = np.zeros((n, head_dim), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
-    rc = lib.oracle_attend_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(s), _ptr(cq), _ptr(ck),
-                                B, num_qo_heads, num_kv_heads, head_dim, float(sm_scale),
-                                int(bool(causal)), int(window), n, _ptr(r), _ptr(out), _ptr(lse))
+    if fp8:
+        ks, vs = _f64(k_scale), _f64(v_scale)
+        rc = lib.oracle_attend_rows_fp8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs), _ptr(s),
+                                        _ptr(cq), _ptr(ck), B, num_qo_heads, num_kv_heads,
+                                        head_dim, float(sm_scale), int(bool(causal)),
+                                        int(window), n, _ptr(r), _ptr(out), _ptr(lse))
+    else:
+        rc = lib.oracle_attend_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(s), _ptr(cq), _ptr(ck),
+                                    B, num_qo_heads, num_kv_heads, head_dim, float(sm_scale),
+                                    int(bool(causal)), int(window), n, _ptr(r), _ptr(out),
+                                    _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attend_rows rejected the problem")
     return out, lse
 
 
 def split_partials(q, k, v, cu_q, cu_k, num_qo_heads, num_kv_heads, head_dim,
-                   sm_scale, causal, window, num_splits):
+                   sm_scale, causal, window, num_splits, k_scale=None, v_scale=None):
     """Per-chunk (acc, m, d) of the split-KV method, no sink.
 
     Returns acc [total_q, Hq, S, d], m [total_q, Hq, S], d [total_q, Hq, S],
@@ -149,7 +194,9 @@ def split_partials(q, k, v, cu_q, cu_k, num_qo_heads, num_kv_heads, head_dim,
     shorter, later ones empty).
     """
     lib = _load()
-    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    fp8 = _is_codes(k)
+    qb = _bits(q)
+    kb, vb = (_codes(k), _codes(v)) if fp8 else (_bits(k), _bits(v))
     cq, ck = _i32(cu_q), _i32(cu_k)
     B = len(cq) - 1
     T = int(cq[-1])
@@ -157,9 +204,17 @@ def split_partials(q, k, v, cu_q, cu_k, num_qo_heads, num_kv_heads, head_dim,
     acc = np.zeros((T, num_qo_heads, S, head_dim), dtype=np.float64)
     m = np.zeros((T, num_qo_heads, S), dtype=np.float64)
     dd = np.zeros((T, num_qo_heads, S), dtype=np.float64)
-    rc = lib.oracle_split_partials(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck), B,
-                                   num_qo_heads, num_kv_heads, head_dim, float(sm_scale),
-                                   int(bool(causal)), int(window), S, _ptr(acc), _ptr(m), _ptr(dd))
+    if fp8:
+        ks, vs = _f64(k_scale), _f64(v_scale)
+        rc = lib.oracle_split_partials_fp8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs),
+                                           _ptr(cq), _ptr(ck), B, num_qo_heads, num_kv_heads,
+                                           head_dim, float(sm_scale), int(bool(causal)),
+                                           int(window), S, _ptr(acc), _ptr(m), _ptr(dd))
+    else:
+        rc = lib.oracle_split_partials(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck), B,
+                                       num_qo_heads, num_kv_heads, head_dim, float(sm_scale),
+                                       int(bool(causal)), int(window), S, _ptr(acc), _ptr(m),
+                                       _ptr(dd))
     if rc != 0:
         raise ValueError("oracle_split_partials rejected the problem")
     return acc, m, dd

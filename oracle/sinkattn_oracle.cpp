@@ -36,6 +36,12 @@
 //    scale, never multiplied by it);
 //  * lse = M + ln Z includes the sink column;
 //  * no keys and no sink (s = -inf): out = 0, lse = -inf.
+//
+// FP8 KV entry points (oracle_attend_rows_fp8, oracle_split_partials_fp8):
+// K and V hold e4m3 codes (the OCP 8-bit floating-point format E4M3: sign,
+// 4-bit exponent with bias 7, 3-bit mantissa, exponent 0 subnormal, the code
+// S.1111.111 NaN, no infinities), and KV head g's values are code * k_scale[g]
+// (keys) and code * v_scale[g] (values). Everything else is as above.
 
 #include <cmath>
 #include <cstdint>
@@ -65,17 +71,40 @@ double bf16_bits_to_double(uint16_t bits) {
 
 const double kNegInf = -std::numeric_limits<double>::infinity();
 
+// e4m3 code -> value, from the format's definition.
+double e4m3_to_double(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const int bias = (ORACLE_PLANT == 10) ? 8 : 7;
+  const double mag = (e == 0) ? std::ldexp(m / 8.0, 1 - bias) : std::ldexp(1.0 + m / 8.0, e - bias);
+  return sign ? -mag : mag;
+}
+
 struct Problem {
   const uint16_t* q;      // [total_q, Hq, d]
-  const uint16_t* k;      // ragged HND: sequence b at element Hkv*cu_k[b]*d, [Hkv, Lk_b, d]
-  const uint16_t* v;      // same layout as k
+  const void* k;          // ragged HND: sequence b at element Hkv*cu_k[b]*d, [Hkv, Lk_b, d]
+  const void* v;          // same layout as k
   const double* sinks;    // [Hq] or nullptr (no sink column)
   const int32_t* cu_q;    // [B+1]
   const int32_t* cu_k;    // [B+1]
   int B, Hq, Hkv, d;
   double scale;
   int causal, window;
+  // K/V element type: bf16 bits, or e4m3 codes with per-KV-head scales
+  int fp8 = 0;
+  const double* k_scale = nullptr;   // [Hkv]
+  const double* v_scale = nullptr;   // [Hkv]
 };
+
+// Element e of the K (or V) array, as a value of KV head g.
+double kv_elem(const Problem& P, const void* base, int64_t e, int g, bool is_v) {
+  if (P.fp8) {
+    const bool use_v = (ORACLE_PLANT == 9) ? !is_v : is_v;
+    return e4m3_to_double(static_cast<const uint8_t*>(base)[e]) *
+           (use_v ? P.v_scale[g] : P.k_scale[g]);
+  }
+  return bf16_bits_to_double(static_cast<const uint16_t*>(base)[e]);
+}
 
 bool key_visible(const Problem& P, int64_t j, int64_t pos) {
   if (P.causal && j > pos) return false;
@@ -94,19 +123,21 @@ double logit(const Problem& P, int b, int64_t tok, int h, int64_t j) {
   const int kvh = (ORACLE_PLANT == 3) ? h % P.Hkv : h / G;
   const int64_t Lk = P.cu_k[b + 1] - P.cu_k[b];
   const uint16_t* qrow = P.q + (tok * P.Hq + h) * static_cast<int64_t>(P.d);
-  const uint16_t* krow =
-      P.k + (static_cast<int64_t>(P.Hkv) * P.cu_k[b] + kvh * Lk + j) * P.d;
+  const int64_t krow = (static_cast<int64_t>(P.Hkv) * P.cu_k[b] + kvh * Lk + j) * P.d;
   double s = 0.0;
-  for (int c = 0; c < P.d; ++c) s += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+  for (int c = 0; c < P.d; ++c)
+    s += bf16_bits_to_double(qrow[c]) * kv_elem(P, P.k, krow + c, kvh, false);
   if (ORACLE_PLANT == 7) return s;
   return P.scale * s;
 }
 
-const uint16_t* value_row(const Problem& P, int b, int h, int64_t j) {
+// Value row of key j for query head h: element c is kv_elem(P, P.v, row + c, g, true).
+int64_t value_row(const Problem& P, int b, int h, int64_t j, int* g) {
   const int G = P.Hq / P.Hkv;
   const int kvh = (ORACLE_PLANT == 3) ? h % P.Hkv : h / G;
   const int64_t Lk = P.cu_k[b + 1] - P.cu_k[b];
-  return P.v + (static_cast<int64_t>(P.Hkv) * P.cu_k[b] + kvh * Lk + j) * P.d;
+  *g = kvh;
+  return (static_cast<int64_t>(P.Hkv) * P.cu_k[b] + kvh * Lk + j) * P.d;
 }
 
 int sequence_of(const Problem& P, int64_t tok) {
@@ -149,8 +180,9 @@ void attend_row(const Problem& P, int64_t tok, int h, double* out, double* lse) 
   for (size_t t = 0; t < l.size(); ++t) {
     const double w = std::exp(l[t] - M);
     Z += w;
-    const uint16_t* vr = value_row(P, b, h, idx[t]);
-    for (int c = 0; c < P.d; ++c) acc[c] += w * bf16_bits_to_double(vr[c]);
+    int g = 0;
+    const int64_t vr = value_row(P, b, h, idx[t], &g);
+    for (int c = 0; c < P.d; ++c) acc[c] += w * kv_elem(P, P.v, vr + c, g, true);
   }
   // The sink's value row is zero: it contributes to Z only.
   for (int c = 0; c < P.d; ++c) out[c] = acc[c] / Z;
@@ -181,8 +213,9 @@ void chunk_partial(const Problem& P, int64_t tok, int h, int64_t lo, int64_t hi,
   for (size_t t = 0; t < l.size(); ++t) {
     const double w = std::exp(l[t] - m);
     dsum += w;
-    const uint16_t* vr = value_row(P, b, h, idx[t]);
-    for (int c = 0; c < P.d; ++c) acc[c] += w * bf16_bits_to_double(vr[c]);
+    int g = 0;
+    const int64_t vr = value_row(P, b, h, idx[t], &g);
+    for (int c = 0; c < P.d; ++c) acc[c] += w * kv_elem(P, P.v, vr + c, g, true);
   }
   *m_out = m;
   *d_out = dsum;
@@ -193,6 +226,7 @@ int check_problem(const Problem& P) {
   if (P.B < 0 || P.Hq <= 0 || P.Hkv <= 0 || P.d <= 0) return 1;
   if (P.Hq % P.Hkv != 0) return 1;
   if (P.window > 0 && !P.causal) return 1;
+  if (P.fp8 && (!P.k_scale || !P.v_scale)) return 1;
   for (int b = 0; b < P.B; ++b) {
     if (P.cu_q[b + 1] < P.cu_q[b] || P.cu_k[b + 1] < P.cu_k[b]) return 1;
     if (P.cu_q[b + 1] - P.cu_q[b] > P.cu_k[b + 1] - P.cu_k[b]) return 1;
@@ -218,13 +252,15 @@ int oracle_num_threads(void) {
 //         [total_q, Hq] in order.
 //   out:  [n_rows, d] float64; lse: [n_rows] float64.
 // Returns 0, or 1 on an invalid problem.
-int oracle_attend_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       const double* sinks, const int32_t* cu_q, const int32_t* cu_k,
-                       int B, int Hq, int Hkv, int d, double sm_scale, int causal,
-                       int window, int64_t n_rows, const int64_t* rows, double* out,
-                       double* lse) {
-  Problem P{q, k, v, sinks, cu_q, cu_k, B, Hq, Hkv, d, sm_scale, causal, window};
+}  // extern "C"
+
+namespace {
+
+int attend_rows(const Problem& P, int64_t n_rows, const int64_t* rows, double* out,
+                double* lse) {
   if (check_problem(P)) return 1;
+  const int B = P.B, Hq = P.Hq, d = P.d;
+  const int32_t* cu_q = P.cu_q;
   const int64_t total_rows = static_cast<int64_t>(cu_q[B]) * Hq;
   if (!rows) n_rows = total_rows;
   for (int64_t r = 0; r < (rows ? n_rows : 0); ++r)
@@ -237,18 +273,55 @@ int oracle_attend_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   return 0;
 }
 
+}  // namespace
+
+extern "C" {
+
+int oracle_attend_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const double* sinks, const int32_t* cu_q, const int32_t* cu_k,
+                       int B, int Hq, int Hkv, int d, double sm_scale, int causal,
+                       int window, int64_t n_rows, const int64_t* rows, double* out,
+                       double* lse) {
+  Problem P{q, k, v, sinks, cu_q, cu_k, B, Hq, Hkv, d, sm_scale, causal, window};
+  return attend_rows(P, n_rows, rows, out, lse);
+}
+
+// The same with K and V as e4m3 codes (uint8, same layout) and per-KV-head
+// scales k_scale, v_scale [Hkv].
+int oracle_attend_rows_fp8(const uint16_t* q, const uint8_t* k, const uint8_t* v,
+                           const double* k_scale, const double* v_scale, const double* sinks,
+                           const int32_t* cu_q, const int32_t* cu_k, int B, int Hq, int Hkv,
+                           int d, double sm_scale, int causal, int window, int64_t n_rows,
+                           const int64_t* rows, double* out, double* lse) {
+  Problem P{q, k, v, sinks, cu_q, cu_k, B, Hq, Hkv, d, sm_scale, causal, window};
+  P.fp8 = 1;
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  return attend_rows(P, n_rows, rows, out, lse);
+}
+
+// Value of every e4m3 code (256 entries; NaN codes give NaN).
+int oracle_e4m3_table(double* out) {
+  for (int c = 0; c < 256; ++c) out[c] = e4m3_to_double(static_cast<uint8_t>(c));
+  return 0;
+}
+
 // Per-chunk partials of the split-KV method, without the sink. Sequence b's
 // keys are cut into num_splits chunks of c = 64 * ceil(Lk_b / (64 * num_splits))
 // keys (ceil(Lk_b / num_splits) rounded up to whole 64-key tiles); chunk s
 // covers [s*c, min((s+1)*c, Lk_b)) and may be empty.
 //   part_acc: [total_q, Hq, S, d]; part_m, part_d: [total_q, Hq, S].
-int oracle_split_partials(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                          const int32_t* cu_q, const int32_t* cu_k, int B, int Hq,
-                          int Hkv, int d, double sm_scale, int causal, int window,
-                          int num_splits, double* part_acc, double* part_m,
-                          double* part_d) {
-  Problem P{q, k, v, nullptr, cu_q, cu_k, B, Hq, Hkv, d, sm_scale, causal, window};
+}  // extern "C"
+
+namespace {
+
+int split_partials(const Problem& P, int num_splits, double* part_acc, double* part_m,
+                   double* part_d) {
   if (check_problem(P) || num_splits < 1) return 1;
+  const int Hq = P.Hq, d = P.d;
+  const int32_t* cu_q = P.cu_q;
+  const int32_t* cu_k = P.cu_k;
+  const int B = P.B;
   const int64_t total_rows = static_cast<int64_t>(cu_q[B]) * Hq;
   const int S = num_splits;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -266,6 +339,32 @@ int oracle_split_partials(const uint16_t* q, const uint16_t* k, const uint16_t* 
     }
   }
   return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_split_partials(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const int32_t* cu_q, const int32_t* cu_k, int B, int Hq,
+                          int Hkv, int d, double sm_scale, int causal, int window,
+                          int num_splits, double* part_acc, double* part_m,
+                          double* part_d) {
+  Problem P{q, k, v, nullptr, cu_q, cu_k, B, Hq, Hkv, d, sm_scale, causal, window};
+  return split_partials(P, num_splits, part_acc, part_m, part_d);
+}
+
+int oracle_split_partials_fp8(const uint16_t* q, const uint8_t* k, const uint8_t* v,
+                              const double* k_scale, const double* v_scale,
+                              const int32_t* cu_q, const int32_t* cu_k, int B, int Hq,
+                              int Hkv, int d, double sm_scale, int causal, int window,
+                              int num_splits, double* part_acc, double* part_m,
+                              double* part_d) {
+  Problem P{q, k, v, nullptr, cu_q, cu_k, B, Hq, Hkv, d, sm_scale, causal, window};
+  P.fp8 = 1;
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  return split_partials(P, num_splits, part_acc, part_m, part_d);
 }
 
 // Partial state of explicit chunk bounds [lo, hi) for one row; used by the

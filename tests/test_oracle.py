@@ -387,3 +387,60 @@ def test_row_subset_matches_full(oracle_lib):
                             True, rows=rows)
     np.testing.assert_array_equal(sub, full[rows])
     np.testing.assert_array_equal(ls, lf[rows])
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV: the decode of the codes, and the scales' use
+# ---------------------------------------------------------------------------
+def test_e4m3_decode_matches_torch_float8(oracle_lib):
+    """Every e4m3 code decodes to torch's float8_e4m3fn value (NaN codes to NaN)."""
+    got = oracle.e4m3_table()
+    want = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    assert (np.isnan(got) == np.isnan(want)).all()
+    fin = ~np.isnan(want)
+    np.testing.assert_array_equal(got[fin], want[fin])
+    # a few values fixed by the format: largest normal, smallest normal and subnormal
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9
+
+
+def _fp8_case(seed, Hkv):
+    """Random e4m3 codes (no NaN) for K and V and power-of-two scales per KV
+    head, plus the bf16 tensors of exactly the dequantised values."""
+    inp = workloads.explicit_inputs([3, 1, 5], [40, 7, 90], 4 * Hkv, Hkv, 64, seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double()
+    valid = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    kc = valid[torch.randint(len(valid), inp["k"].shape, generator=g)]
+    vc = valid[torch.randint(len(valid), inp["v"].shape, generator=g)]
+    ks = torch.tensor([2.0 ** (-3 + (i % 4)) for i in range(Hkv)], dtype=torch.float64)
+    vs = torch.tensor([2.0 ** (1 - (i % 3)) for i in range(Hkv)], dtype=torch.float64)
+    cu = inp["cu_k"].tolist()
+    heads = torch.cat([torch.arange(Hkv).repeat_interleave(cu[b + 1] - cu[b])
+                       for b in range(len(cu) - 1)])
+    kb = (table[kc.long()] * ks[heads][:, None]).to(torch.bfloat16)
+    vb = (table[vc.long()] * vs[heads][:, None]).to(torch.bfloat16)
+    # the dequantised values are exact in bf16 (4 significant bits, small exponents)
+    assert torch.equal(kb.double(), table[kc.long()] * ks[heads][:, None])
+    return inp, kc, vc, ks, vs, kb, vb
+
+
+def test_fp8_oracle_equals_bf16_oracle_on_exactly_representable_values(oracle_lib):
+    """With power-of-two scales the dequantised K/V are exact bf16 values: the
+    FP8 path (codes x per-head scales) must give the bf16 path's result on
+    them, for full rows and for split partials; distinct key / value scales
+    per KV head check which scale goes where."""
+    Hkv = 3
+    inp, kc, vc, ks, vs, kb, vb = _fp8_case(5, Hkv)
+    Hq, d = 4 * Hkv, 64
+    args = (inp["cu_q"], inp["cu_k"], Hq, Hkv, d, 0.2, True, 0)
+    o8, l8 = oracle.attend(inp["q"], kc, vc, inp["sinks"], *args, k_scale=ks, v_scale=vs)
+    ob, lb = oracle.attend(inp["q"], kb, vb, inp["sinks"], *args)
+    np.testing.assert_allclose(o8, ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l8, lb, rtol=0, atol=1e-12)
+    a8, m8, d8 = oracle.split_partials(inp["q"], kc, vc, inp["cu_q"], inp["cu_k"], Hq, Hkv, d,
+                                       0.2, True, 0, 3, k_scale=ks, v_scale=vs)
+    ab, mb, db = oracle.split_partials(inp["q"], kb, vb, inp["cu_q"], inp["cu_k"], Hq, Hkv, d,
+                                       0.2, True, 0, 3)
+    np.testing.assert_allclose(a8, ab, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(m8, mb)
+    np.testing.assert_allclose(d8, db, rtol=0, atol=1e-12)

@@ -23,6 +23,8 @@ PLANTS = {
     6: "merge counts the sink once per split",
     7: "sm_scale not applied to the logits",
     8: "lse excludes the sink column",
+    9: "FP8 keys scaled by the value scale and values by the key scale",
+    10: "e4m3 exponent bias 8 instead of 7",
 }
 
 
