@@ -5,6 +5,7 @@ Public API (thin wrappers over the C ABI in ``include/sinkattn.h``):
 ``sinkattn_decode``, ``sinkattn_decode_fused``, ``sinkattn_decode_noalloc``, ``sinkattn_decode_workspace_bytes``,
 ``sinkattn_decode_default_splits``, ``sinkattn_prefill_paged``,
 ``sinkattn_decode_split_paged``, ``sinkattn_decode_paged`` (paged KV cache),
+``sinkattn_decode_split_fp8``, ``sinkattn_decode_fp8`` (FP8 e4m3 KV cache),
 ``sinkattn_status_string``,
 ``sinkattn_last_error``, ``sinkattn_debug_status``, ``sinkattn_set_decode_kernel``,
 ``sinkattn_set_prefill_kernel``.
@@ -18,10 +19,12 @@ from ._binding import (  # noqa: F401
     sinkattn_debug_status,
     sinkattn_decode,
     sinkattn_decode_default_splits,
+    sinkattn_decode_fp8,
     sinkattn_decode_fused,
     sinkattn_decode_noalloc,
     sinkattn_decode_paged,
     sinkattn_decode_split,
+    sinkattn_decode_split_fp8,
     sinkattn_decode_split_paged,
     sinkattn_decode_workspace_bytes,
     sinkattn_last_error,

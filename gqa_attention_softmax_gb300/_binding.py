@@ -68,11 +68,16 @@ def lib() -> ctypes.CDLL:
             L.sinkattn_debug_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
             L.sinkattn_set_decode_kernel.argtypes = [ctypes.c_int]
             L.sinkattn_set_prefill_kernel.argtypes = [ctypes.c_int]
+            L.sinkattn_decode_split_fp8.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32,
+                                                    F, I32, I32, I32, P, P, P]
+            L.sinkattn_decode_fp8.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, F,
+                                              I32, I32, I32, P, P, SZ, P, P, P]
             for name in ("sinkattn_prefill", "sinkattn_decode_split", "sinkattn_merge",
                          "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc",
                          "sinkattn_decode_workspace_bytes", "sinkattn_decode_default_splits",
                          "sinkattn_debug_status", "sinkattn_set_decode_kernel",
-                         "sinkattn_set_prefill_kernel",
+                         "sinkattn_set_prefill_kernel", "sinkattn_decode_split_fp8",
+                         "sinkattn_decode_fp8",
                          "sinkattn_prefill_paged", "sinkattn_decode_split_paged",
                          "sinkattn_decode_paged"):
                 getattr(L, name).restype = ctypes.c_int
@@ -323,6 +328,53 @@ def sinkattn_set_decode_kernel(kind) -> None:
     "tcgen05" (or the integer codes of include/sinkattn.h)."""
     code = DECODE_KERNELS[kind] if isinstance(kind, str) else int(kind)
     _check(lib().sinkattn_set_decode_kernel(code))
+
+
+def sinkattn_decode_split_fp8(q, k, v, k_scale, v_scale, kv_indptr, q_len, max_kv_len,
+                              num_splits, sm_scale=None, causal=True, window=0, part_acc=None,
+                              part_md=None, stream=None):
+    """sinkattn_decode_split over an FP8 KV cache: k, v uint8 e4m3 codes in
+    the ragged HND layout [Hkv * total_k, d]; k_scale, v_scale fp32 [Hkv]
+    per-KV-head scales (device). Returns (part_acc, part_md) without the sink."""
+    rows, Hq, d = q.shape
+    Hkv = k_scale.numel()
+    batch = kv_indptr.numel() - 1
+    if part_acc is None:
+        part_acc = torch.empty((rows, Hq, num_splits, d), dtype=torch.float32, device=q.device)
+    if part_md is None:
+        part_md = torch.empty((rows, Hq, num_splits, 2), dtype=torch.float32, device=q.device)
+    rc = lib().sinkattn_decode_split_fp8(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_scale), _ptr(v_scale), _ptr(kv_indptr), batch,
+        int(q_len), int(max_kv_len), Hq, Hkv, d, _scale(sm_scale, d), int(bool(causal)),
+        int(window), int(num_splits), _ptr(part_acc), _ptr(part_md), _stream(q, stream))
+    _check(rc)
+    return part_acc, part_md
+
+
+def sinkattn_decode_fp8(q, k, v, k_scale, v_scale, kv_indptr, sinks, q_len, max_kv_len,
+                        num_splits=0, sm_scale=None, causal=True, window=0, workspace=None,
+                        out=None, lse=None, return_lse=True, stream=None):
+    """sinkattn_decode over an FP8 KV cache (layout as in
+    sinkattn_decode_split_fp8). Returns (out, lse)."""
+    rows, Hq, d = q.shape
+    Hkv = k_scale.numel()
+    batch = kv_indptr.numel() - 1
+    if num_splits <= 0:
+        num_splits = sinkattn_decode_default_splits(batch, q_len, Hq, Hkv, d, max_kv_len)
+    need = sinkattn_decode_workspace_bytes(batch, q_len, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
+    rc = lib().sinkattn_decode_fp8(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_scale), _ptr(v_scale), _ptr(kv_indptr), batch,
+        int(q_len), int(max_kv_len), Hq, Hkv, d, _scale(sm_scale, d), int(bool(causal)),
+        int(window), int(num_splits), _ptr(sinks), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(q, stream))
+    _check(rc)
+    return out, lse
 
 
 PREFILL_KERNELS = {"auto": 0, "one_block": 1, "persistent": 2}

@@ -79,6 +79,28 @@ int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int
   return SINKATTN_OK;
 }
 
+int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return SINKATTN_CUDA_ERROR;
+  }
+  if (rows == 0) rows = 1;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (u8) failed (CUresult %d)", static_cast<int>(r));
+    return SINKATTN_CUDA_ERROR;
+  }
+  return SINKATTN_OK;
+}
+
 int make_q_tmap(CUtensorMap* map, const void* q, uint64_t total_q, int Hq, int d, int G, int QB) {
   auto fn = encode_fn();
   if (!fn) {
@@ -292,8 +314,19 @@ int decode_args(const void* q, const void* k, const void* v, const int32_t* kv_i
 }
 
 // Partials with the selected kernel (a.part_acc / a.part_md set).
+// FP8 KV: e4m3 K/V codes and their per-KV-head scales.
+struct Fp8Kv {
+  const float* k_scale;
+  const float* v_scale;
+};
+
 int launch_partials(const AttnArgs& a, cudaStream_t stream) {
   const int kind = g_decode_kernel.load(std::memory_order_relaxed);
+  if (a.kv_fp8) {   // the warp-level kernel carries the FP8 path
+    if (kind == SINKATTN_DECODE_TCGEN05)
+      return fail(SINKATTN_UNSUPPORTED, "the tcgen05 decode kernel has no FP8 KV path");
+    return launch_attn_mma(a, stream);
+  }
   const bool tc_ok = decode_tc_supported(a);
   if (kind == SINKATTN_DECODE_TCGEN05 && !tc_ok)
     return fail(SINKATTN_UNSUPPORTED,
@@ -307,7 +340,8 @@ int decode_split_impl(const void* q, const void* k, const void* v, const int32_t
                       const PagedKv* pg, int32_t batch, int32_t q_len, int32_t max_kv_len,
                       int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                       float sm_scale, int32_t causal, int32_t window, int32_t num_splits,
-                      float* part_acc, float* part_md, void* stream) {
+                      float* part_acc, float* part_md, void* stream,
+                      const Fp8Kv* f8 = nullptr) {
   g_last_error[0] = '\0';
   AttnArgs a;
   int rc = decode_args(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads, num_kv_heads,
@@ -316,6 +350,14 @@ int decode_split_impl(const void* q, const void* k, const void* v, const int32_t
   if (pg && (rc = check_paged(*pg, num_kv_heads))) return rc;
   if (!part_acc || !part_md || !aligned16(part_acc) || !aligned16(part_md))
     return fail(SINKATTN_INVALID_ARG, "partial buffers must be non-null and 16-byte aligned");
+  if (f8) {
+    if (!f8->k_scale || !f8->v_scale ||
+        (reinterpret_cast<uintptr_t>(f8->k_scale) | reinterpret_cast<uintptr_t>(f8->v_scale)) & 3u)
+      return fail(SINKATTN_INVALID_ARG, "k_scale and v_scale must be non-null and 4-byte aligned");
+    a.kv_fp8 = 1;
+    a.k_scale = f8->k_scale;
+    a.v_scale = f8->v_scale;
+  }
   if (batch == 0) return SINKATTN_OK;
   a.part_acc = part_acc; a.part_md = part_md;
   set_paged(&a, pg);
@@ -326,7 +368,8 @@ int decode_impl(const void* q, const void* k, const void* v, const int32_t* kv_i
                 const PagedKv* pg, int32_t batch, int32_t q_len, int32_t max_kv_len,
                 int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, float sm_scale,
                 int32_t causal, int32_t window, int32_t num_splits, const float* sinks,
-                void* workspace, size_t workspace_bytes, void* out, float* lse, void* stream) {
+                void* workspace, size_t workspace_bytes, void* out, float* lse, void* stream,
+                const Fp8Kv* f8 = nullptr) {
   g_last_error[0] = '\0';
   int rc;
   if (num_splits <= 0) {
@@ -350,7 +393,7 @@ int decode_impl(const void* q, const void* k, const void* v, const int32_t* kv_i
                                             ((slots * head_dim * 4 + 255) & ~static_cast<size_t>(255)));
   rc = decode_split_impl(q, k, v, kv_indptr, pg, batch, q_len, max_kv_len, num_qo_heads,
                          num_kv_heads, head_dim, sm_scale, causal, window, num_splits, part_acc,
-                         part_md, stream);
+                         part_md, stream, f8);
   if (rc) return rc;
   if (batch == 0) return SINKATTN_OK;
   // the partials are this call's scratch: the merge may drop them from L2
@@ -383,6 +426,30 @@ int sinkattn_decode_split_paged(const void* q, const void* k_pages, const void* 
   return decode_split_impl(q, k_pages, v_pages, kv_indptr, &pg, batch, q_len, max_kv_len,
                            num_qo_heads, num_kv_heads, head_dim, sm_scale, causal, window,
                            num_splits, part_acc, part_md, stream);
+}
+
+int sinkattn_decode_split_fp8(const void* q, const void* k, const void* v,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                              int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                              int32_t head_dim, float sm_scale, int32_t causal, int32_t window,
+                              int32_t num_splits, float* part_acc, float* part_md, void* stream) {
+  const Fp8Kv f8{k_scale, v_scale};
+  return decode_split_impl(q, k, v, kv_indptr, nullptr, batch, q_len, max_kv_len, num_qo_heads,
+                           num_kv_heads, head_dim, sm_scale, causal, window, num_splits, part_acc,
+                           part_md, stream, &f8);
+}
+
+int sinkattn_decode_fp8(const void* q, const void* k, const void* v, const float* k_scale,
+                        const float* v_scale, const int32_t* kv_indptr, int32_t batch,
+                        int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
+                        int32_t num_kv_heads, int32_t head_dim, float sm_scale, int32_t causal,
+                        int32_t window, int32_t num_splits, const float* sinks, void* workspace,
+                        size_t workspace_bytes, void* out, float* lse, void* stream) {
+  const Fp8Kv f8{k_scale, v_scale};
+  return decode_impl(q, k, v, kv_indptr, nullptr, batch, q_len, max_kv_len, num_qo_heads,
+                     num_kv_heads, head_dim, sm_scale, causal, window, num_splits, sinks,
+                     workspace, workspace_bytes, out, lse, stream, &f8);
 }
 
 int sinkattn_set_prefill_kernel(int kind) {

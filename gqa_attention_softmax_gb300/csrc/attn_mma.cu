@@ -14,6 +14,12 @@
 //  * Per tile: S = Q K^T on mma.sync, mask, online softmax (running max and
 //    sum per row, max reduced over the 4-lane quads with warp shuffles),
 //    O += P V with P re-packed to bf16 straight from the S accumulators.
+//  * FP8 KV (e4m3 codes, per-KV-head scales): the producer's TMA copies the
+//    raw codes into their own stage ring; two converter warps widen each tile
+//    to f16 (exact: f16 holds every e4m3 value) in the same 128-byte-swizzled
+//    layout, and the consumers run the f16 form of the same MMAs with Q
+//    converted to f16 once. The key scale joins the logit scale, the value
+//    scale multiplies the chunk's accumulator.
 //  * Tiles are right-aligned to the end of the CTA's key range, so no copy
 //    ever reads past the last key the CTA needs; keys before the range that a
 //    tile covers are masked (and are real data or TMA zero-fill, never NaN).
@@ -59,20 +65,28 @@ struct MmaParams {
   int page_size, box_rows;
   const int32_t* page_indptr;
   const int32_t* page_indices;
+  // FP8 KV: per-KV-head scales of the e4m3 codes
+  const float* k_scale;
+  const float* v_scale;
 };
 
-template <int D, int RT, int TG, int KT, int NST>
+template <int D, int RT, int TG, int KT, int NST, bool FP8 = false>
 struct MmaCfg {
   static constexpr int NW = RT * TG;               // consumer warps
-  static constexpr int THREADS = (NW + 1) * 32;    // + producer warp
+  static constexpr int NCONV = FP8 ? 2 : 0;        // e4m3 -> f16 converter warps
+  static constexpr int THREADS = (NW + 1 + NCONV) * 32;   // + producer warp
   static constexpr int NSUB = D / 64;              // 64-column sub-tiles
   static constexpr int SUB_BYTES = KT * 128;
   static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int F8_TILE = KT * D;           // one K or V tile of e4m3 codes
+  static constexpr int F8_STAGE = 2 * F8_TILE;
+  static constexpr int OFF_F8 = NST * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_F8 + (FP8 ? NST * F8_STAGE : 0);
   static constexpr int XCHG_FLOATS_PER_LANE = D / 2 + 4;
   static constexpr int XCHG_BYTES = (TG - 1) * RT * 32 * XCHG_FLOATS_PER_LANE * 4;
-  static constexpr int BAR_BYTES = 2 * NST * 8 + 16;
-  static constexpr int SMEM_BYTES = 1024 + NST * STAGE_BYTES + BAR_BYTES + XCHG_BYTES;
+  static constexpr int BAR_BYTES = 4 * NST * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES + XCHG_BYTES;
   // fused mode: one CTA's partial, [16 RT rows][m, d, pad, pad, acc[D]], over the tile ring
   static constexpr int XOUT_STRIDE = D + 4;
   static_assert(16 * RT * XOUT_STRIDE * 4 <= NST * STAGE_BYTES, "partial fits in the tile ring");
@@ -81,11 +95,12 @@ struct MmaCfg {
   static constexpr int MIN_CTAS = 2;
 };
 
-template <int D, int RT, int TG, int KT, int NST, bool FUSED>
-__global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D, RT, TG, KT, NST>::MIN_CTAS)
+template <int D, int RT, int TG, int KT, int NST, bool FUSED, bool FP8>
+__global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
+                                  MmaCfg<D, RT, TG, KT, NST, FP8>::MIN_CTAS)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const MmaParams p) {
-  using C = MmaCfg<D, RT, TG, KT, NST>;
+  using C = MmaCfg<D, RT, TG, KT, NST, FP8>;
   constexpr int NW = C::NW;
   constexpr float NEG_INF = kNegInf;
 
@@ -93,10 +108,13 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE_BYTES);
+  uint8_t* f8 = smem + C::OFF_F8;        // FP8: e4m3 stage ring [NST][K | V]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NST;
-  int* abort_flag = reinterpret_cast<int*>(empty + NST);
-  float* xchg = reinterpret_cast<float*>(smem + NST * C::STAGE_BYTES + C::BAR_BYTES);
+  uint64_t* f8_full = empty + NST;       // FP8: codes of the stage landed
+  uint64_t* f8_empty = f8_full + NST;    // FP8: codes of the stage converted
+  int* abort_flag = reinterpret_cast<int*>(f8_empty + NST);
+  float* xchg = reinterpret_cast<float*>(smem + C::OFF_BAR + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -135,8 +153,10 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], FP8 ? C::NCONV : 1);
       mbar_init(&empty[i], RT);
+      mbar_init(&f8_full[i], 1);
+      mbar_init(&f8_empty[i], C::NCONV > 0 ? C::NCONV : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -169,12 +189,36 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NST;
         const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
+        const int j0 = first + i * KT;
+        if constexpr (FP8) {
+          // e4m3 codes into the code ring; the converter warps fill `full`
+          if (!__all_sync(members, mbar_wait(&f8_empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
+            break;
+          uint8_t* kc = f8 + st * C::F8_STAGE;
+          uint8_t* vc = kc + C::F8_TILE;
+          if (leader) mbar_arrive_expect_tx(&f8_full[st], C::F8_STAGE);
+          if (!paged) {
+            tma_load_2d_hint(kc, &tmK, 0, slab + j0, &f8_full[st], policy);
+            tma_load_2d_hint(vc, &tmV, 0, slab + j0, &f8_full[st], policy);
+          } else {
+            const int nbox = KT / p.box_rows;
+            const int a = j0 + min(lane, nbox - 1) * p.box_rows;
+            const int page = pc.get(j0 / p.page_size, a / p.page_size, lane);
+            if (lane < nbox) {
+              const int row = (page * p.Hkv + kvh) * p.page_size + a % p.page_size;
+              const int off = (a - j0) * D;
+              tma_load_2d_hint(kc + off, &tmK, 0, row, &f8_full[st], policy);
+              tma_load_2d_hint(vc + off, &tmV, 0, row, &f8_full[st], policy);
+            }
+          }
+          issued = i + 1;
+          continue;
+        }
         if (!__all_sync(members, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
           break;
         uint8_t* kt = tiles + st * C::STAGE_BYTES;
         uint8_t* vt = kt + C::TILE_BYTES;
         if (leader) mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-        const int j0 = first + i * KT;
         if (!paged) {
 #pragma unroll
           for (int sub = 0; sub < C::NSUB; ++sub) {
@@ -201,7 +245,53 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
       }
       if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
         for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_drain(&full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
+          mbar_drain(FP8 ? &f8_full[i % NST] : &full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
+      }
+    }
+  } else if (FP8 && warp > NW) {
+    // ------------------------------------------------------------ converters
+    // Warps NW+1 and NW+2 widen each tile's e4m3 codes to f16, one 16-byte
+    // chunk (16 codes) per step, into the 128-byte-swizzled tile the
+    // consumers read; they hand the tile over on `full` and the codes back on
+    // f8_empty.
+    const int ct = static_cast<int>(threadIdx.x) - (NW + 1) * 32;   // 0 .. 63
+    constexpr int CH_ROW = D / 16;        // 16-byte chunks per row of codes
+    constexpr int CH_TILE = KT * CH_ROW;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % NST;
+      const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&f8_full[st], ph, abort_flag, &g_status_attn_mma)))
+        break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
+        break;
+      const uint8_t* codes = f8 + st * C::F8_STAGE;
+      uint8_t* dst = tiles + st * C::STAGE_BYTES;
+#pragma unroll 4
+      for (int c = ct; c < 2 * CH_TILE; c += 64) {
+        const int tensor = c / CH_TILE;   // 0: K, 1: V
+        const int rem = c - tensor * CH_TILE;
+        const int row = rem / CH_ROW, cb = rem - row * CH_ROW;
+        const uint4 w =
+            *reinterpret_cast<const uint4*>(codes + tensor * C::F8_TILE + row * D + cb * 16);
+        uint4 h0, h1;
+        h0.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x));
+        h0.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16));
+        h0.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y));
+        h0.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16));
+        h1.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z));
+        h1.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16));
+        h1.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w));
+        h1.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16));
+        // columns 16 cb .. 16 cb + 15: sub-tile cb / 4, 16-byte chunks 2 (cb % 4) and + 1
+        uint8_t* sub = dst + tensor * C::TILE_BYTES + (cb >> 2) * C::SUB_BYTES;
+        const int ch = (cb & 3) * 2;
+        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch)) = h0;
+        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch + 1)) = h1;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&f8_empty[st]);
+        mbar_arrive(&full[st]);
       }
     }
   } else {
@@ -230,10 +320,13 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
     for (int reg = 0; reg < 4; ++reg) {
       const int i = reg & 1;
       const int col = kk * 16 + (lane & 3) * 2 + ((reg >> 1) << 3);
-      qa[kk][reg] = valid[i]
+      uint32_t qv = valid[i]
                         ? *reinterpret_cast<const uint32_t*>(
                               p.q + (static_cast<size_t>(tok[i]) * p.Hq + head[i]) * D + col)
                         : 0u;
+      if constexpr (FP8)   // f16 operands: bf16 -> f32 (exact) -> f16
+        qv = pack_f16x2(__uint_as_float(qv << 16), __uint_as_float(qv & 0xffff0000u));
+      qa[kk][reg] = qv;
     }
   }
 
@@ -248,7 +341,10 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
     l[i] = 0.f;
   }
 
-  const float c2 = p.scale_log2;
+  // logits in raw units q . k (k the e4m3 value with FP8 KV); c2 turns them
+  // into base-2 exponents
+  const float kscale = FP8 ? p.k_scale[kvh] : 1.f;
+  const float c2 = p.scale_log2 * kscale;
   for (int i = tg; i < ntiles; i += TG) {
     const int st = i % NST;
     const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
@@ -270,8 +366,13 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
         const int chunk = 2 * kk + (lane >> 3);
         uint32_t bf[4];
         ldsm_x4(bf, kbase + (chunk >> 3) * C::SUB_BYTES + sw128_offset(trow, chunk & 7));
-        mma_bf16_16816(s[j], qa[kk], bf[0], bf[1]);
-        mma_bf16_16816(s[j], qa[kk + 1], bf[2], bf[3]);
+        if constexpr (FP8) {
+          mma_f16_16816(s[j], qa[kk], bf[0], bf[1]);
+          mma_f16_16816(s[j], qa[kk + 1], bf[2], bf[3]);
+        } else {
+          mma_bf16_16816(s[j], qa[kk], bf[0], bf[1]);
+          mma_bf16_16816(s[j], qa[kk + 1], bf[2], bf[3]);
+        }
       }
     }
 
@@ -332,10 +433,17 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
 #pragma unroll
     for (int kt2 = 0; kt2 < KT / 16; ++kt2) {
       uint32_t a[4];
-      a[0] = pack_bf16x2(s[2 * kt2][0], s[2 * kt2][1]);
-      a[1] = pack_bf16x2(s[2 * kt2][2], s[2 * kt2][3]);
-      a[2] = pack_bf16x2(s[2 * kt2 + 1][0], s[2 * kt2 + 1][1]);
-      a[3] = pack_bf16x2(s[2 * kt2 + 1][2], s[2 * kt2 + 1][3]);
+      if constexpr (FP8) {
+        a[0] = pack_f16x2(s[2 * kt2][0], s[2 * kt2][1]);
+        a[1] = pack_f16x2(s[2 * kt2][2], s[2 * kt2][3]);
+        a[2] = pack_f16x2(s[2 * kt2 + 1][0], s[2 * kt2 + 1][1]);
+        a[3] = pack_f16x2(s[2 * kt2 + 1][2], s[2 * kt2 + 1][3]);
+      } else {
+        a[0] = pack_bf16x2(s[2 * kt2][0], s[2 * kt2][1]);
+        a[1] = pack_bf16x2(s[2 * kt2][2], s[2 * kt2][3]);
+        a[2] = pack_bf16x2(s[2 * kt2 + 1][0], s[2 * kt2 + 1][1]);
+        a[3] = pack_bf16x2(s[2 * kt2 + 1][2], s[2 * kt2 + 1][3]);
+      }
 #pragma unroll
       for (int jd = 0; jd < D / 8; jd += 2) {
         const int mi = lane >> 3;
@@ -343,8 +451,13 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
         const int chunk = jd + (mi >> 1);
         uint32_t bf[4];
         ldsm_x4_trans(bf, vbase + (chunk >> 3) * C::SUB_BYTES + sw128_offset(trow, chunk & 7));
-        mma_bf16_16816(o[jd], a, bf[0], bf[1]);
-        mma_bf16_16816(o[jd + 1], a, bf[2], bf[3]);
+        if constexpr (FP8) {
+          mma_f16_16816(o[jd], a, bf[0], bf[1]);
+          mma_f16_16816(o[jd + 1], a, bf[2], bf[3]);
+        } else {
+          mma_bf16_16816(o[jd], a, bf[0], bf[1]);
+          mma_bf16_16816(o[jd + 1], a, bf[2], bf[3]);
+        }
       }
     }
     __syncwarp();
@@ -403,6 +516,8 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
 
   // ------------------------------------------------------------------ epilogue
   if (!FUSED && writer) {
+    // FP8: the value scale turns the accumulator into value units
+    const float vscale = FP8 ? p.v_scale[kvh] : 1.f;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       if (!valid[i]) continue;
@@ -411,11 +526,12 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
 #pragma unroll
       for (int jd = 0; jd < D / 8; ++jd) {
         const int col = jd * 8 + (lane & 3) * 2;
-        *reinterpret_cast<float2*>(arow + col) = make_float2(o[jd][2 * i], o[jd][2 * i + 1]);
+        *reinterpret_cast<float2*>(arow + col) =
+            make_float2(o[jd][2 * i] * vscale, o[jd][2 * i + 1] * vscale);
       }
       if ((lane & 3) == 0) {
         float2 md;
-        md.x = (m[i] == NEG_INF) ? NEG_INF : m[i] * p.sm_scale;
+        md.x = (m[i] == NEG_INF) ? NEG_INF : m[i] * (p.sm_scale * kscale);
         md.y = l[i];
         *reinterpret_cast<float2*>(p.part_md + (rowid * S + split) * 2) = md;
       }
@@ -509,15 +625,15 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST>::THREADS, MmaCfg<D,
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int D, int RT, int TG, int KT, int NST, bool FUSED>
+template <int D, int RT, int TG, int KT, int NST, bool FUSED, bool FP8>
 static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
-  using C = MmaCfg<D, RT, TG, KT, NST>;
+  using C = MmaCfg<D, RT, TG, KT, NST, FP8>;
   CUtensorMap tmK, tmV;
   const uint64_t rows = kv_map_rows(a);
   const int box = kv_box_rows(a, KT);
-  int rc = make_rows_tmap(&tmK, a.k, rows, D, box, 128);
+  int rc = FP8 ? make_rows_tmap_u8(&tmK, a.k, rows, D, box) : make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
-  rc = make_rows_tmap(&tmV, a.v, rows, D, box, 128);
+  rc = FP8 ? make_rows_tmap_u8(&tmV, a.v, rows, D, box) : make_rows_tmap(&tmV, a.v, rows, D, box, 128);
   if (rc) return rc;
 
   MmaParams p{};
@@ -546,8 +662,10 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   p.sinks = a.sinks;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
 
-  auto kern = attn_mma_kernel<D, RT, TG, KT, NST, FUSED>;
+  auto kern = attn_mma_kernel<D, RT, TG, KT, NST, FUSED, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) {
@@ -589,7 +707,7 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   return SINKATTN_OK;
 }
 
-template <bool FUSED>
+template <bool FUSED, bool FP8>
 static int launch_attn_mma_t(const AttnArgs& a, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   const int rows = G * a.q_len;
@@ -599,23 +717,24 @@ static int launch_attn_mma_t(const AttnArgs& a, cudaStream_t stream) {
     return SINKATTN_UNSUPPORTED;
   }
   if (a.d == 64) {
-    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4, FUSED>(a, stream);
-    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4, FUSED>(a, stream);
-    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4, FUSED>(a, stream);
-    return launch_cfg<64, 4, 2, 64, 4, FUSED>(a, stream);
+    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4, FUSED, FP8>(a, stream);
+    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4, FUSED, FP8>(a, stream);
+    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4, FUSED, FP8>(a, stream);
+    return launch_cfg<64, 4, 2, 64, 4, FUSED, FP8>(a, stream);
   }
-  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4, FUSED>(a, stream);
-  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4, FUSED>(a, stream);
-  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4, FUSED>(a, stream);
-  return launch_cfg<128, 4, 2, 32, 4, FUSED>(a, stream);
+  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4, FUSED, FP8>(a, stream);
+  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4, FUSED, FP8>(a, stream);
+  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4, FUSED, FP8>(a, stream);
+  return launch_cfg<128, 4, 2, 32, 4, FUSED, FP8>(a, stream);
 }
 
 int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
-  return launch_attn_mma_t<false>(a, stream);
+  return a.kv_fp8 ? launch_attn_mma_t<false, true>(a, stream)
+                  : launch_attn_mma_t<false, false>(a, stream);
 }
 
 int launch_attn_mma_fused(const AttnArgs& a, cudaStream_t stream) {
-  return launch_attn_mma_t<true>(a, stream);
+  return launch_attn_mma_t<true, false>(a, stream);
 }
 
 int read_status_attn_mma(cudaStream_t s, int* status) {

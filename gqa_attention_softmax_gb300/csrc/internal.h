@@ -35,6 +35,11 @@ struct AttnArgs {
   int32_t num_pages;
   const int32_t* page_indptr;   // [B+1]
   const int32_t* page_indices;  // [page_indptr[B]]
+  // FP8 KV (kv_fp8 != 0): k and v hold e4m3 codes (one byte per element, same
+  // layout); KV head g's keys are code * k_scale[g], values code * v_scale[g]
+  int32_t kv_fp8;
+  const float* k_scale;         // [Hkv], device
+  const float* v_scale;         // [Hkv], device
 };
 
 // Rows of the 2-D tensor map over K or V, and the box height: contiguous HND
@@ -56,6 +61,9 @@ inline int kv_box_rows(const AttnArgs& a, int tile_keys) {
 // boxes and 128-byte swizzling. Returns 0 or a SINKATTN_* status.
 int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
                    int swizzle_bytes);
+// The same over a [rows, d] array of bytes (e4m3 codes), [box_rows, d] boxes,
+// no swizzle.
+int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows);
 
 // Encodes a 3-D tensor map over q [total_q, Hq, d] bf16 whose box is
 // [QB tokens][G heads][64 columns] (128 rows of one GQA group), 128-byte swizzled.

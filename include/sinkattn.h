@@ -299,6 +299,41 @@ SINKATTN_API int sinkattn_decode_paged(const void* q, const void* k_pages, const
                                        size_t workspace_bytes, void* out, float* lse,
                                        void* stream);
 
+/*
+ * FP8 KV cache: sinkattn_decode_split and sinkattn_decode with K and V held
+ * as e4m3 codes (the OCP 8-bit floating-point format E4M3, one byte per
+ * element, in the same ragged HND layout) and per-KV-head fp32 scales:
+ *   k, v:     uint8 codes [Hkv * total_k, d] (device);
+ *   k_scale:  float [Hkv] (device): key j of KV head g is code * k_scale[g];
+ *   v_scale:  float [Hkv] (device): value j of KV head g is code * v_scale[g].
+ * Every other argument, layout, result, the partials and the merge are those
+ * of the bf16 entry points ("GPT-OSS on Day 0", section "Kernels for GPT-OSS /
+ * Sink attention", with the keys and values dequantised). The kernel widens
+ * the codes to f16, which holds every e4m3 value exactly, and runs the
+ * products in f16 with q converted to f16: |q| must stay below 65504, and
+ * q elements below 2^-14 in magnitude lose relative precision. The partials
+ * come from the warp-level kernel (SINKATTN_DECODE_TCGEN05 returns
+ * SINKATTN_UNSUPPORTED). k_scale / v_scale null or misaligned:
+ * SINKATTN_INVALID_ARG.
+ */
+SINKATTN_API int sinkattn_decode_split_fp8(const void* q, const void* k, const void* v,
+                                           const float* k_scale, const float* v_scale,
+                                           const int32_t* kv_indptr, int32_t batch,
+                                           int32_t q_len, int32_t max_kv_len,
+                                           int32_t num_qo_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, float sm_scale, int32_t causal,
+                                           int32_t window, int32_t num_splits, float* part_acc,
+                                           float* part_md, void* stream);
+SINKATTN_API int sinkattn_decode_fp8(const void* q, const void* k, const void* v,
+                                     const float* k_scale, const float* v_scale,
+                                     const int32_t* kv_indptr, int32_t batch, int32_t q_len,
+                                     int32_t max_kv_len, int32_t num_qo_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, float sm_scale,
+                                     int32_t causal, int32_t window, int32_t num_splits,
+                                     const float* sinks, void* workspace,
+                                     size_t workspace_bytes, void* out, float* lse,
+                                     void* stream);
+
 /* Human-readable name of a status code (static string). */
 SINKATTN_API const char* sinkattn_status_string(int status);
 

@@ -209,3 +209,12 @@ def test_prefill_kernel_switch(L):
     assert L.sinkattn_set_prefill_kernel(-1) == 1
     for k in (1, 2, 0):
         assert L.sinkattn_set_prefill_kernel(k) == 0
+
+
+def test_decode_split_fp8_rejects_missing_scales(L):
+    rc = L.sinkattn_decode_split_fp8(A, B, C, None, 0x9000, 0x5000, 2, 1, 100, 8, 1, 128, 0.1, 1,
+                                     0, 4, 0x7000, 0x8000, None)
+    assert rc == 1 and "scale" in sa.sinkattn_last_error()
+    rc = L.sinkattn_decode_split_fp8(A, B, C, 0x9002, 0x9000, 0x5000, 2, 1, 100, 8, 1, 128, 0.1,
+                                     1, 0, 4, 0x7000, 0x8000, None)
+    assert rc == 1
