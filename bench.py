@@ -33,7 +33,8 @@ import torch  # noqa: E402
 
 HEADLINE = "gptoss_decode"
 ALSO = ["qwen_mtp_decode", "gptoss_prefill", "gptoss_prefill_w128", "qwen_prefill",
-        "gptoss_decode_paged", "qwen_mtp_decode_paged"]
+        "gptoss_decode_paged", "qwen_mtp_decode_paged", "gptoss_decode_fp8",
+        "qwen_mtp_decode_fp8"]
 METRIC = "decode KV-read HBM GB/s and prefill TFLOP/s, each as % of GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2**20
@@ -68,8 +69,10 @@ def work(w, inp):
         kv_tok = sum(min(lk, lq + w.window - 1) for lq, lk in zip(inp["q_lens"], inp["kv_lens"]))
     else:
         kv_tok = sum(inp["kv_lens"])
-    kv_bytes = 2 * Hkv * kv_tok * d * 2
+    kv_bytes = 2 * Hkv * kv_tok * d * (1 if w.kv_fp8 else 2)
     small = Hq * 4 + (inp["batch"] + 1) * 4 * (1 if w.kind == "decode" else 2)
+    if w.kv_fp8:          # per-KV-head key and value scales
+        small += 2 * Hkv * 4
     if w.page_size > 0:   # page lists
         small += 4 * (inp["batch"] + 1 + sum(-(-lk // w.page_size) for lk in inp["kv_lens"]))
     total = q_bytes + kv_bytes + q_bytes + tq * Hq * 4 + small
@@ -195,7 +198,12 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
         _sync(dist_ctx)
         s0.record(stream)
         for _ in range(steps):
-            if w.page_size > 0:
+            if w.kv_fp8:
+                B.sinkattn_decode_split_fp8(inp["q"], inp["k_fp8"], inp["v_fp8"], inp["k_scale"],
+                                            inp["v_scale"], inp["cu_k"], w.q_len, inp["max_k"],
+                                            run.num_splits, w.scale, w.causal, w.window,
+                                            part_acc=acc, part_md=md)
+            elif w.page_size > 0:
                 B.sinkattn_decode_split_paged(inp["q"], inp["k_pages"], inp["v_pages"], inp["cu_k"],
                                               inp["page_indptr"], inp["page_indices"], w.q_len,
                                               inp["max_k"], run.num_splits, w.scale, w.causal,
@@ -398,13 +406,15 @@ def reference_arm(args, rank, world):
 
 def decode_kernel_name(w):
     """The split kernel the library's default selection runs for this shape."""
+    if w.kv_fp8:
+        return "attn_mma_kernel (mma.sync f16, e4m3 codes widened in shared memory)"
     return "decode_tc_kernel (tcgen05)" if w.head_dim == 128 else "attn_mma_kernel (mma.sync)"
 
 
 def _workload_desc(w):
     if w.kind == "decode":
         layout = ("paged HND bf16, %d-key pages in random order" % w.page_size if w.page_size > 0
-                  else "HND bf16")
+                  else "HND FP8 e4m3 with per-KV-head scales" if w.kv_fp8 else "HND bf16")
         return ("%s: batch %d, %d query / %d KV heads, head_dim %d, q_len %d, kv_len ~ U[%d, %d], "
                 "%s, fp32 sinks" % (w.name, w.batch, w.num_qo_heads, w.num_kv_heads,
                                     w.head_dim, w.q_len, w.kv_range[0], w.kv_range[1], layout))

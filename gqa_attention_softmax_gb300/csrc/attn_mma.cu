@@ -15,11 +15,11 @@
 //    sum per row, max reduced over the 4-lane quads with warp shuffles),
 //    O += P V with P re-packed to bf16 straight from the S accumulators.
 //  * FP8 KV (e4m3 codes, per-KV-head scales): the producer's TMA copies the
-//    raw codes into their own stage ring; two converter warps widen each tile
-//    to f16 (exact: f16 holds every e4m3 value) in the same 128-byte-swizzled
-//    layout, and the consumers run the f16 form of the same MMAs with Q
-//    converted to f16 once. The key scale joins the logit scale, the value
-//    scale multiplies the chunk's accumulator.
+//    raw codes into the stage ring; the warps of the token group that owns a
+//    tile widen it to f16 (exact: f16 holds every e4m3 value) into their own
+//    128-byte-swizzled tile buffer and run the f16 form of the same MMAs on
+//    it, with Q converted to f16 once. The key scale joins the logit scale,
+//    the value scale multiplies the chunk's accumulator.
 //  * Tiles are right-aligned to the end of the CTA's key range, so no copy
 //    ever reads past the last key the CTA needs; keys before the range that a
 //    tile covers are masked (and are real data or TMA zero-fill, never NaN).
@@ -73,19 +73,20 @@ struct MmaParams {
 template <int D, int RT, int TG, int KT, int NST, bool FP8 = false>
 struct MmaCfg {
   static constexpr int NW = RT * TG;               // consumer warps
-  static constexpr int NCONV = FP8 ? 2 : 0;        // e4m3 -> f16 converter warps
-  static constexpr int THREADS = (NW + 1 + NCONV) * 32;   // + producer warp
+  static constexpr int THREADS = (NW + 1) * 32;    // + producer warp
   static constexpr int NSUB = D / 64;              // 64-column sub-tiles
   static constexpr int SUB_BYTES = KT * 128;
   static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int F8_TILE = KT * D;           // one K or V tile of e4m3 codes
   static constexpr int F8_STAGE = 2 * F8_TILE;
-  static constexpr int OFF_F8 = NST * STAGE_BYTES;
+  // bf16: the stage ring of tiles; FP8: one f16 tile buffer per token group,
+  // then the ring of e4m3 stages
+  static constexpr int OFF_F8 = FP8 ? TG * STAGE_BYTES : NST * STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_F8 + (FP8 ? NST * F8_STAGE : 0);
   static constexpr int XCHG_FLOATS_PER_LANE = D / 2 + 4;
   static constexpr int XCHG_BYTES = (TG - 1) * RT * 32 * XCHG_FLOATS_PER_LANE * 4;
-  static constexpr int BAR_BYTES = 4 * NST * 8 + 16;
+  static constexpr int BAR_BYTES = (2 * NST + 2 * TG) * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES + XCHG_BYTES;
   // fused mode: one CTA's partial, [16 RT rows][m, d, pad, pad, acc[D]], over the tile ring
   static constexpr int XOUT_STRIDE = D + 4;
@@ -107,13 +108,14 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* tiles = smem;
+  uint8_t* tiles = smem;                 // bf16: stage ring; FP8: f16 buffer per token group
   uint8_t* f8 = smem + C::OFF_F8;        // FP8: e4m3 stage ring [NST][K | V]
+  // bf16: full / empty of the stage ring; FP8: codes landed / codes read
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NST;
-  uint64_t* f8_full = empty + NST;       // FP8: codes of the stage landed
-  uint64_t* f8_empty = f8_full + NST;    // FP8: codes of the stage converted
-  int* abort_flag = reinterpret_cast<int*>(f8_empty + NST);
+  uint64_t* cvt_done = empty + NST;      // FP8, RT > 1: [TG] the group's tile is converted
+  uint64_t* buf_free = cvt_done + TG;    // FP8, RT > 1: [TG] the group's buffer was read
+  int* abort_flag = reinterpret_cast<int*>(buf_free + TG);
   float* xchg = reinterpret_cast<float*>(smem + C::OFF_BAR + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5;
@@ -153,10 +155,12 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], FP8 ? C::NCONV : 1);
+      mbar_init(&full[i], 1);
       mbar_init(&empty[i], RT);
-      mbar_init(&f8_full[i], 1);
-      mbar_init(&f8_empty[i], C::NCONV > 0 ? C::NCONV : 1);
+    }
+    for (int i = 0; i < TG; ++i) {
+      mbar_init(&cvt_done[i], RT);
+      mbar_init(&buf_free[i], RT);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -192,14 +196,14 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         const int j0 = first + i * KT;
         if constexpr (FP8) {
           // e4m3 codes into the code ring; the converter warps fill `full`
-          if (!__all_sync(members, mbar_wait(&f8_empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
+          if (!__all_sync(members, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
             break;
           uint8_t* kc = f8 + st * C::F8_STAGE;
           uint8_t* vc = kc + C::F8_TILE;
-          if (leader) mbar_arrive_expect_tx(&f8_full[st], C::F8_STAGE);
+          if (leader) mbar_arrive_expect_tx(&full[st], C::F8_STAGE);
           if (!paged) {
-            tma_load_2d_hint(kc, &tmK, 0, slab + j0, &f8_full[st], policy);
-            tma_load_2d_hint(vc, &tmV, 0, slab + j0, &f8_full[st], policy);
+            tma_load_2d_hint(kc, &tmK, 0, slab + j0, &full[st], policy);
+            tma_load_2d_hint(vc, &tmV, 0, slab + j0, &full[st], policy);
           } else {
             const int nbox = KT / p.box_rows;
             const int a = j0 + min(lane, nbox - 1) * p.box_rows;
@@ -207,8 +211,8 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
             if (lane < nbox) {
               const int row = (page * p.Hkv + kvh) * p.page_size + a % p.page_size;
               const int off = (a - j0) * D;
-              tma_load_2d_hint(kc + off, &tmK, 0, row, &f8_full[st], policy);
-              tma_load_2d_hint(vc + off, &tmV, 0, row, &f8_full[st], policy);
+              tma_load_2d_hint(kc + off, &tmK, 0, row, &full[st], policy);
+              tma_load_2d_hint(vc + off, &tmV, 0, row, &full[st], policy);
             }
           }
           issued = i + 1;
@@ -245,53 +249,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
       }
       if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
         for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_drain(FP8 ? &f8_full[i % NST] : &full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
-      }
-    }
-  } else if (FP8 && warp > NW) {
-    // ------------------------------------------------------------ converters
-    // Warps NW+1 and NW+2 widen each tile's e4m3 codes to f16, one 16-byte
-    // chunk (16 codes) per step, into the 128-byte-swizzled tile the
-    // consumers read; they hand the tile over on `full` and the codes back on
-    // f8_empty.
-    const int ct = static_cast<int>(threadIdx.x) - (NW + 1) * 32;   // 0 .. 63
-    constexpr int CH_ROW = D / 16;        // 16-byte chunks per row of codes
-    constexpr int CH_TILE = KT * CH_ROW;
-    for (int i = 0; i < ntiles; ++i) {
-      const int st = i % NST;
-      const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&f8_full[st], ph, abort_flag, &g_status_attn_mma)))
-        break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
-        break;
-      const uint8_t* codes = f8 + st * C::F8_STAGE;
-      uint8_t* dst = tiles + st * C::STAGE_BYTES;
-#pragma unroll 4
-      for (int c = ct; c < 2 * CH_TILE; c += 64) {
-        const int tensor = c / CH_TILE;   // 0: K, 1: V
-        const int rem = c - tensor * CH_TILE;
-        const int row = rem / CH_ROW, cb = rem - row * CH_ROW;
-        const uint4 w =
-            *reinterpret_cast<const uint4*>(codes + tensor * C::F8_TILE + row * D + cb * 16);
-        uint4 h0, h1;
-        h0.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x));
-        h0.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16));
-        h0.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y));
-        h0.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16));
-        h1.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z));
-        h1.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16));
-        h1.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w));
-        h1.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16));
-        // columns 16 cb .. 16 cb + 15: sub-tile cb / 4, 16-byte chunks 2 (cb % 4) and + 1
-        uint8_t* sub = dst + tensor * C::TILE_BYTES + (cb >> 2) * C::SUB_BYTES;
-        const int ch = (cb & 3) * 2;
-        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch)) = h0;
-        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch + 1)) = h1;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&f8_empty[st]);
-        mbar_arrive(&full[st]);
+          mbar_drain(&full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
       }
     }
   } else {
@@ -348,8 +306,58 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
   for (int i = tg; i < ntiles; i += TG) {
     const int st = i % NST;
     const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
-    if (!mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma)) break;
-    const uint32_t kbase = smem_u32(tiles + st * C::STAGE_BYTES);
+    uint32_t kbase;
+    if constexpr (FP8) {
+      // Widen this tile's e4m3 codes into the group's f16 buffer: each of the
+      // group's RT warps converts every RT-th 16-byte chunk (16 codes).
+      const int nt = i / TG;   // the group's tile ordinal
+      uint8_t* fb = tiles + tg * C::STAGE_BYTES;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma))) break;
+      if constexpr (RT > 1) {   // every warp of the group has read the previous tile
+        if (nt > 0 && !__all_sync(0xffffffffu, mbar_wait(&buf_free[tg], (nt - 1) & 1, abort_flag,
+                                                         &g_status_attn_mma)))
+          break;
+      } else {
+        __syncwarp();
+      }
+      const uint8_t* codes = f8 + st * C::F8_STAGE;
+      constexpr int CH_ROW = D / 16;        // 16-byte chunks per row of codes
+      constexpr int CH_TILE = KT * CH_ROW;
+#pragma unroll 4
+      for (int c = rt * 32 + lane; c < 2 * CH_TILE; c += RT * 32) {
+        const int tensor = c / CH_TILE;   // 0: K, 1: V
+        const int rem = c - tensor * CH_TILE;
+        const int row = rem / CH_ROW, cb = rem - row * CH_ROW;
+        const uint4 w =
+            *reinterpret_cast<const uint4*>(codes + tensor * C::F8_TILE + row * D + cb * 16);
+        uint4 h0, h1;
+        h0.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x));
+        h0.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16));
+        h0.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y));
+        h0.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16));
+        h1.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z));
+        h1.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16));
+        h1.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w));
+        h1.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16));
+        // columns 16 cb .. 16 cb + 15: sub-tile cb / 4, 16-byte chunks 2 (cb % 4) and + 1
+        uint8_t* sub = fb + tensor * C::TILE_BYTES + (cb >> 2) * C::SUB_BYTES;
+        const int ch = (cb & 3) * 2;
+        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch)) = h0;
+        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch + 1)) = h1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);   // this warp's codes are read
+      if constexpr (RT > 1) {
+        if (lane == 0) mbar_arrive(&cvt_done[tg]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&cvt_done[tg], nt & 1, abort_flag,
+                                               &g_status_attn_mma)))
+          break;
+      }
+      kbase = smem_u32(fb);
+    } else {
+      if (!mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma)) break;
+      kbase = smem_u32(tiles + st * C::STAGE_BYTES);
+    }
     const uint32_t vbase = kbase + C::TILE_BYTES;
     const int j0 = first + i * KT;   // key index of tile row 0
 
@@ -461,7 +469,11 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if constexpr (FP8) {
+      if (RT > 1 && lane == 0) mbar_arrive(&buf_free[tg]);   // the group's buffer is read
+    } else {
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
   }
 
   // Row sums are split over the 4 lanes of each quad.

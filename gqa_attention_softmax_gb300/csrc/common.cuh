@@ -6,7 +6,6 @@
 #include <math.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -172,10 +171,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Two e4m3 codes (low byte first) -> two f16 (low half first), exact.
+// Two e4m3 codes (low byte first) -> two f16 (low half first), exact: one
+// conversion instruction straight into the packed register.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(codes, __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

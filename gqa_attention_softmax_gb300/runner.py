@@ -35,7 +35,7 @@ class Runner:
         # (sinkattn_decode_fused) is available but measured slower on the
         # gpt-oss- and Qwen-shaped decodes, so it is opt-in.
         self.fused = (w.kind == "decode" and fused and self.num_splits <= 16
-                      and w.page_size == 0)
+                      and w.page_size == 0 and not w.kv_fp8)
         self.workspace = None
         if w.kind == "decode" and not self.fused:
             n = B.sinkattn_decode_workspace_bytes(inp["batch"], w.q_len, w.num_qo_heads, w.head_dim,
@@ -53,6 +53,13 @@ class Runner:
                                            i["max_k"], w.num_kv_heads, num_splits=self.num_splits,
                                            sm_scale=w.scale, causal=w.causal, window=w.window,
                                            out=self.out, lse=self.lse, stream=stream)
+        if w.kind == "decode" and w.kv_fp8:
+            return B.sinkattn_decode_fp8(i["q"], i["k_fp8"], i["v_fp8"], i["k_scale"],
+                                         i["v_scale"], i["cu_k"], i["sinks"], w.q_len, i["max_k"],
+                                         num_splits=self.num_splits, sm_scale=w.scale,
+                                         causal=w.causal, window=w.window,
+                                         workspace=self.workspace, out=self.out, lse=self.lse,
+                                         stream=stream)
         if w.kind == "decode" and w.page_size > 0:
             return B.sinkattn_decode_paged(i["q"], i["k_pages"], i["v_pages"], i["cu_k"],
                                            i["page_indptr"], i["page_indices"], i["sinks"],

@@ -58,6 +58,7 @@ class Workload:
     sm_scale: Optional[float] = None  # None -> 1/sqrt(head_dim)
     seed: int = 0
     page_size: int = 0              # > 0: K/V also scattered into page pools (paged decode)
+    kv_fp8: bool = False            # K/V also quantised to e4m3 codes (FP8 decode)
 
     @property
     def scale(self) -> float:
@@ -86,6 +87,13 @@ WORKLOADS = {
     # Qwen3-235B-shaped MTP speculative decode: 3 drafts, 16 KV chunks.
     "qwen_mtp_decode": Workload("qwen_mtp_decode", "decode", 64, 4, 128, True, batch=256, q_len=3,
                                 kv_range=(4000, 8000), num_splits=16, sink_dist="uniform2"),
+    # The two decodes over an FP8 (e4m3) KV cache with per-KV-head scales.
+    "gptoss_decode_fp8": Workload("gptoss_decode_fp8", "decode", 64, 8, 64, True, batch=64,
+                                  q_len=1, kv_range=(1024, 8192), sink_dist="uniform2",
+                                  sm_scale=1.0 / 8.0, kv_fp8=True),
+    "qwen_mtp_decode_fp8": Workload("qwen_mtp_decode_fp8", "decode", 64, 4, 128, True,
+                                    batch=256, q_len=3, kv_range=(4000, 8000), num_splits=16,
+                                    sink_dist="uniform2", kv_fp8=True),
     # The two decodes over a paged KV cache (pages in seeded random order).
     "gptoss_decode_paged": Workload("gptoss_decode_paged", "decode", 64, 8, 64, True, batch=64,
                                     q_len=1, kv_range=(1024, 8192), sink_dist="uniform2",
@@ -158,6 +166,8 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
     )
     if w.page_size > 0:
         inp.update(to_paged(inp, Hkv, w.page_size, seed=seed, spare_pages=0, fill_scale=0.0))
+    if w.kv_fp8:
+        inp.update(to_fp8(inp, Hkv))
     return inp
 
 
