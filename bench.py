@@ -407,6 +407,9 @@ def reference_arm(args, rank, world):
 def decode_kernel_name(w):
     """The split kernel the library's default selection runs for this shape."""
     if w.kv_fp8:
+        g = w.num_qo_heads // w.num_kv_heads
+        if w.head_dim == 128 and g <= 64:
+            return "decode_tc_kernel (tcgen05 f16, e4m3 codes widened in shared memory)"
         return "attn_mma_kernel (mma.sync f16, e4m3 codes widened in shared memory)"
     return "decode_tc_kernel (tcgen05)" if w.head_dim == 128 else "attn_mma_kernel (mma.sync)"
 

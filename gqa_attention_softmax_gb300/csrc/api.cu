@@ -322,9 +322,13 @@ struct Fp8Kv {
 
 int launch_partials(const AttnArgs& a, cudaStream_t stream) {
   const int kind = g_decode_kernel.load(std::memory_order_relaxed);
-  if (a.kv_fp8) {   // the warp-level kernel carries the FP8 path
-    if (kind == SINKATTN_DECODE_TCGEN05)
-      return fail(SINKATTN_UNSUPPORTED, "the tcgen05 decode kernel has no FP8 KV path");
+  if (a.kv_fp8) {   // tcgen05 up to 64 rows per tile at head_dim 128, else the warp-level kernel
+    const bool tc8 = decode_tc_supported(a);
+    if (kind == SINKATTN_DECODE_TCGEN05 && !tc8)
+      return fail(SINKATTN_UNSUPPORTED,
+                  "the tcgen05 FP8 decode needs head_dim 128 and at most 64 heads per group");
+    if (kind == SINKATTN_DECODE_TCGEN05 || (kind == SINKATTN_DECODE_AUTO && tc8))
+      return launch_decode_tc(a, stream);
     return launch_attn_mma(a, stream);
   }
   const bool tc_ok = decode_tc_supported(a);

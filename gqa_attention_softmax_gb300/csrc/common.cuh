@@ -184,6 +184,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Sum of the two f16 halves of a packed pair, in fp32 (exact widening).
+__device__ __forceinline__ float f16x2_sum(uint32_t v) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+  return f.x + f.y;
+}
+
 // Sum of the two bf16 halves of a packed pair, in fp32 (exact widening).
 __device__ __forceinline__ float bf16x2_sum(uint32_t v) {
   return __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);

@@ -57,6 +57,9 @@ struct DtcParams {
   int page_size, box_rows;
   const int32_t* page_indptr;
   const int32_t* page_indices;
+  // FP8 KV: per-KV-head scales of the e4m3 codes
+  const float* k_scale;
+  const float* v_scale;
 };
 
 // One work item: (sequence b, KV head, query block, KV chunk) and its keys.
@@ -101,7 +104,7 @@ __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* c
   return t;
 }
 
-template <int RR>
+template <int RR, bool FP8 = false>
 struct DtcCfg {
   static constexpr int D = 128;
   static constexpr int KT = 64;                 // keys per KV tile
@@ -114,22 +117,37 @@ struct DtcCfg {
   static constexpr int OFF_Q = 0;               // two Q buffers
   static constexpr int OFF_RING = (2 * Q_BUF + 1023) / 1024 * 1024;
   static constexpr int CU_CAP = 2048;           // sequences whose kv_indptr is staged in smem
-  static constexpr int FIXED =
-      OFF_RING + RR * XS * 4 + 2 * 128 * 16 + (CU_CAP + 1) * 4 + 16 + 40 * 8 + 64 + 1024;
+  // FP8: a ring of e4m3 K/V code stages feeds the f16 tile ring
+  static constexpr int CODE_STAGE = 2 * KT * D; // 16 KB
+  static constexpr int NSTF = FP8 ? 2 : 0;   // (two code stages leave room for a deeper f16 ring)
+  static constexpr int NSTF_MOD = FP8 ? NSTF : 1;   // (a non-zero modulus for the bf16 build)
+  static constexpr int FIXED = OFF_RING + RR * XS * 4 + 2 * 128 * 16 + (CU_CAP + 1) * 4 + 16 +
+                               (40 + 2 * NSTF + 2) * 8 + 64 + 1024 + NSTF * CODE_STAGE;
   static constexpr int NST = (232448 - FIXED) / STAGE < 6 ? (232448 - FIXED) / STAGE : 6;
-  static constexpr int OFF_STG = OFF_RING + NST * STAGE;   // [RR][XS] fp32 partial rows
+  static constexpr int OFF_CODE = OFF_RING + NST * STAGE;  // FP8: [NSTF][K | V] codes
+  static constexpr int OFF_STG = OFF_CODE + NSTF * CODE_STAGE;   // [RR][XS] fp32 partial rows
   static constexpr int OFF_ML = OFF_STG + RR * XS * 4;     // [2][128] (m, l, lr) per row
   static constexpr int OFF_CU = OFF_ML + 2 * 128 * 16;     // [CU_CAP + 1] kv_indptr copy
   static constexpr int OFF_BAR = OFF_CU + ((CU_CAP + 1) * 4 + 15) / 16 * 16;
   static constexpr int NSB = 4;                 // S buffers in TMEM
-  static constexpr int N_BARS = 2 + 2 + 2 * NST + 3 * NSB + 2 + 2 + 2 + 1;
+  static constexpr int N_BARS =
+      2 + 2 + 2 * NST + 3 * NSB + 2 + 2 + 2 + 1 + (FP8 ? 2 * NSTF + 2 : 0);
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
-  static constexpr int THREADS = 12 * 32;
+  // bf16: 12 warps (10 producer, 11 MMA); FP8: 14 warps, 8-11 convert, 12 producer, 13 MMA
+  static constexpr int THREADS = (FP8 ? 14 : 12) * 32;
+  static constexpr int W_PROD = FP8 ? 12 : 10;
+  static constexpr int W_MMA = FP8 ? 13 : 11;
+  static constexpr int N_CVT = 4;               // FP8 converter warps
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = NSB * KT;   // O buffers at 256 and 384
   static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
   static_assert(RR % 8 == 0 && RR >= 8 && RR <= 128, "rows");
   static_assert(NST >= 2, "ring depth");
+  static_assert(!FP8 || NST >= 3, "FP8: the f16 ring keeps three tiles for the S look-ahead");
+  // S runs LA tiles ahead of PV: tile g + LA reuses tile g's ring stage at the
+  // latest. FP8 keeps a stage of slack (LA = NST - 1), so the conversion of
+  // tile g + LA starts when PV(g - 1) completes rather than PV(g).
+  static constexpr int LA = FP8 ? NST - 1 : (NST < 3 ? NST : 3);
   // the A operand reads 128 rows from each Q sub-tile: keep them inside the allocation
   static_assert(OFF_Q + Q_BUF + Q_SUB + 128 * 128 <= OFF_BAR, "Q over-read stays in shared memory");
   // one CTA per SM, so the 512-column TMEM allocation always succeeds
@@ -139,12 +157,14 @@ struct DtcCfg {
 // Persistent: CTA c runs items c, c + gridDim.x, ... back to back, so the
 // ring keeps streaming across item boundaries. Warps 0-3 softmax (thread =
 // row = TMEM lane), 4-7 epilogue (read O, write the partial), 10 TMA
-// producer, 11 TMEM allocation + MMA issue (8, 9 idle: the producer and the
-// issuer sit on the SM sub-partitions of the softmax warps with the fewest
-// real rows). Q and O are double-buffered by item; S has four buffers: the
-// issuer keeps S three tiles ahead, issuing S(g+3) right after PV(g) (it
-// reuses P(g-1)'s buffer, whose PV has completed by then), so the chain
-// softmax -> PV -> S spans three tiles of softmax work.
+// producer, 11 TMEM allocation + MMA issue (8, 9 idle for bf16 KV: the
+// producer and the issuer sit on the SM sub-partitions of the softmax warps
+// with the fewest real rows). Q and O are double-buffered by item; S has four
+// buffers: the issuer keeps S three tiles ahead, issuing S(g+3) right after
+// PV(g) (it reuses P(g-1)'s buffer, whose PV has completed by then), so the
+// chain softmax -> PV -> S spans three tiles of softmax work. Tile g+3 takes
+// tile g's ring stage at the latest, so a two-stage ring (128-row tiles)
+// runs two tiles ahead instead.
 //
 // Lazy rescaling: a row's weights are taken relative to a reference maximum
 // that moves only when a score exceeds it by more than 2^8 in exp2 units,
@@ -154,12 +174,20 @@ struct DtcCfg {
 // as (m', lr) with m' = m + ln(l / lr): m' + ln lr is the chunk's exact
 // log-sum-exp and acc / lr its output normalised by the weights actually
 // applied -- the same state, rescaled, as (chunk max, exact sum).
-template <int RR, bool PAGED>
-__global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
+//
+// FP8 KV (e4m3 codes with per-KV-head scales): the producer copies the codes
+// into a ring of code stages; warps 8-11 (one per SM sub-partition) convert
+// each item's Q in place to f16 and widen each tile's codes to f16 into the
+// tile ring (the layout the MMAs read), and every MMA runs on f16 operands (P
+// is packed as f16). The producer moves to warp 12 and the MMA issuer to 13.
+// The key scale joins the item's logit scale, the value scale multiplies the
+// staged accumulator.
+template <int RR, bool PAGED, bool FP8>
+__global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const DtcParams p) {
-  using C = DtcCfg<RR>;
+  using C = DtcCfg<RR, FP8>;
   constexpr int D = C::D, KT = C::KT, NST = C::NST;
   constexpr float NEG_INF = kNegInf;
 
@@ -178,7 +206,10 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
   uint64_t* o_free = o_full + 2;        // [2] by item: epilogue has read O and (m, l)
   uint64_t* ml_full = o_free + 2;       // [2] by item: softmax wrote (m, l) (128 arrivals)
   uint64_t* drain = ml_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* c_full = drain + 1;         // FP8: [NSTF] codes of the stage landed
+  uint64_t* c_empty = c_full + C::NSTF; // FP8: [NSTF] codes of the stage converted
+  uint64_t* q_cvt = c_empty + C::NSTF;  // FP8: [2] the item's Q is f16
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_cvt + (FP8 ? 2 : 0));
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float4* ml = reinterpret_cast<float4*>(smem + C::OFF_ML);
   int* status = &g_status_decode_tc;
@@ -213,14 +244,20 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
       mbar_init(&ml_full[i], 128);
     }
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_full[i], FP8 ? C::N_CVT : 1);   // FP8: the converter warps
       mbar_init(&kv_empty[i], 1);
     }
+    for (int i = 0; i < C::NSTF; ++i) {
+      mbar_init(&c_full[i], 1);
+      mbar_init(&c_empty[i], C::N_CVT);
+    }
+    if (FP8)
+      for (int i = 0; i < 2; ++i) mbar_init(&q_cvt[i], C::N_CVT);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 11) {
+  if (warp == C::W_MMA) {
     tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -232,7 +269,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
   };
 
-  if (warp == 10) {
+  if (warp == C::W_PROD) {
     // ---------------------------------------------------------------- producer
     // Contiguous KV: lane 0 runs the loop alone. Paged KV: the whole warp runs
     // it (page lists are read 32 entries per warp load, lane i issues box i of
@@ -272,11 +309,23 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
         }
         const int slab = t.k_start * p.Hkv + t.kvh * t.Lk;   // contiguous: tensor-map row of key 0
         for (int j = 0; j < t.n; ++j, ++g) {
+          const int j0 = t.first + j * KT;
+          if constexpr (FP8) {
+            // the tile's e4m3 codes into the code ring (the converters fill the tile ring)
+            const int sc = g % C::NSTF_MOD;
+            if (!pwait(&c_empty[sc], ((g / C::NSTF_MOD) & 1) ^ 1)) { ok = false; break; }
+            uint8_t* codes = smem + C::OFF_CODE + sc * C::CODE_STAGE;
+            if (leader) {
+              mbar_arrive_expect_tx(&c_full[sc], C::CODE_STAGE);
+              tma_load_2d_hint(codes, &tmK, 0, slab + j0, &c_full[sc], policy);
+              tma_load_2d_hint(codes + KT * D, &tmV, 0, slab + j0, &c_full[sc], policy);
+            }
+            continue;
+          }
           const int st = g % NST;
           if (!pwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
           uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
           if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-          const int j0 = t.first + j * KT;
           if constexpr (!PAGED) {
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
@@ -307,16 +356,23 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
       }
       if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
         for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
-        for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+        if constexpr (FP8) {
+          for (int i = max(0, g - C::NSTF_MOD); i < g; ++i)
+            mbar_drain(&c_full[i % C::NSTF_MOD], (i / C::NSTF_MOD) & 1);
+        } else {
+          for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+        }
       }
     }
-  } else if (warp == 11) {
+  } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- MMA issuer
     // The whole warp runs the schedule (waits, cursors, descriptor arithmetic
     // stay warp-uniform) and one elected lane issues each MMA and commit.
     const bool leader = tc::elect_one();
-    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KT, false);
-    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
+    constexpr uint32_t idesc_s = FP8 ? tc::idesc_f16_f32(128, KT, false)
+                                     : tc::idesc_bf16_f32(128, KT, false);
+    constexpr uint32_t idesc_o = FP8 ? tc::idesc_f16_f32(128, D, true)
+                                     : tc::idesc_bf16_f32(128, D, true);
     constexpr uint64_t STAGE16 = C::STAGE >> 4;   // descriptor address units
     // A K step (16 elements = 32 bytes) inside a 128-byte swizzle row adds 2
     // to the address field; the next 64-column block adds its sub-tile size.
@@ -327,7 +383,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     const uint64_t vd0 =
         tc::smem_desc_sw128(smem_u32(smem + C::OFF_RING + C::KV_TILE), C::SUB_KV, 1024);
 
-    // S cursor: runs three tiles ahead of the PV cursor (four S buffers).
+    // S cursor: runs LA (three, or two with a two-stage ring) tiles ahead of the PV cursor.
     int sk = 0, sj = 0, sg = 0, sqi = 0;
     DtcItem st_ = n_mine > 0 ? item_of(0) : DtcItem{};
     auto s_skip_empty = [&]() {
@@ -337,7 +393,8 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
       }
     };
     auto issue_next_s = [&]() -> bool {
-      if (sj == 0 && !wwait(&q_full[sqi & 1], (sqi >> 1) & 1)) return false;
+      // the item's Q has landed (FP8: and has been converted to f16)
+      if (sj == 0 && !wwait(FP8 ? &q_cvt[sqi & 1] : &q_full[sqi & 1], (sqi >> 1) & 1)) return false;
       if (!wwait(&kv_full[sg % NST], (sg / NST) & 1)) return false;
       // S(sg) overwrites P(sg - 4): PV(sg - 4) must have read it
       if (sg >= 4 && !wwait(&pv_done[sg & 3], ((sg - 4) >> 2) & 1)) return false;
@@ -370,7 +427,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
 
     bool ok = true;
     s_skip_empty();
-    for (int w = 0; w < 3 && ok && sk < n_mine; ++w) ok = issue_next_s();
+    for (int w = 0; w < C::LA && ok && sk < n_mine; ++w) ok = issue_next_s();
     int g = 0;   // PV cursor: tile ordinal
     for (int k = 0; ok && k < n_mine; ++k) {
       const int n = item_of(k).n;
@@ -394,7 +451,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
           tc::commit(&kv_empty[g % NST]);
         }
         __syncwarp();
-        // S(g+3) into P(g-1)'s buffer: PV(g-1) was issued a tile ago
+        // S(g+LA) into P(g+LA-4)'s buffer: PV(g+LA-4) was issued at least a tile ago
         if (sk < n_mine && !issue_next_s()) { ok = false; break; }
       }
       if (!ok) break;
@@ -405,18 +462,92 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
     if (leader) tc::commit(drain);
     __syncwarp();
     mbar_drain(drain, 0);
+  } else if (FP8 && warp >= 8 && warp < 8 + C::N_CVT) {
+    // ------------------------------------------------------------ converters
+    // Per item: its Q in place, bf16 -> f16 (same swizzled positions); per
+    // tile: 16-byte chunks of e4m3 codes -> f16 into the tile ring stage.
+    // Generic-proxy writes the tensor core reads: fenced before each hand-over.
+    constexpr int NT = C::N_CVT * 32;
+    const int ct = static_cast<int>(threadIdx.x) - 8 * 32;   // 0 .. NT - 1
+    constexpr int CH_ROW = D / 16;          // 16-byte chunks per row of codes
+    constexpr int CH_TILE = KT * CH_ROW;
+    int g = 0, qi = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < n_mine; ++k) {
+      const DtcItem t = item_of(k);
+      if (t.n == 0) continue;
+      if (!wwait(&q_full[qi & 1], (qi >> 1) & 1)) break;
+      uint8_t* qb = smem + C::OFF_Q + (qi & 1) * C::Q_BUF;
+      for (int c = ct; c < C::Q_BUF / 16; c += NT) {
+        uint4 w = *reinterpret_cast<const uint4*>(qb + c * 16);
+        w.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+        w.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+        w.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+        w.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+        *reinterpret_cast<uint4*>(qb + c * 16) = w;
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_cvt[qi & 1]);
+      ++qi;
+      for (int j = 0; j < t.n; ++j, ++g) {
+        const int sc = g % C::NSTF_MOD, st = g % NST;
+        if (!wwait(&c_full[sc], (g / C::NSTF_MOD) & 1)) { ok = false; break; }
+        const uint8_t* codes = smem + C::OFF_CODE + sc * C::CODE_STAGE;
+        uint8_t* dst = smem + C::OFF_RING + st * C::STAGE;
+        // all of this thread's codes into registers first (the loads do not
+        // wait behind the stores), then the code stage is handed back
+        constexpr int PER = 2 * CH_TILE / NT;
+        uint4 w[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int c = ct + i * NT;
+          w[i] = *reinterpret_cast<const uint4*>(codes + c * 16);   // row-major [2][KT][D] codes
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c_empty[sc]);
+        if (!wwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int c = ct + i * NT;
+          const int tensor = c / CH_TILE;   // 0: K, 1: V
+          const int rem = c - tensor * CH_TILE;
+          const int row = rem / CH_ROW, cb = rem - row * CH_ROW;
+          uint4 h0, h1;
+          h0.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].x));
+          h0.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].x >> 16));
+          h0.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].y));
+          h0.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].y >> 16));
+          h1.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].z));
+          h1.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].z >> 16));
+          h1.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].w));
+          h1.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i].w >> 16));
+          // columns 16 cb .. 16 cb + 15: sub-tile cb / 4, 16-byte chunks 2 (cb % 4) and + 1
+          // (lanes cb and cb + 4 of a row share bank groups; an order that
+          // avoids it measured slower)
+          uint8_t* sub = dst + tensor * C::KV_TILE + (cb >> 2) * C::SUB_KV;
+          const int ch = (cb & 3) * 2;
+          *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch)) = h0;
+          *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch + 1)) = h1;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[st]);
+      }
+    }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- softmax
     const int row = warp * 32 + lane;   // TMEM lane; warp w owns lanes 32w..32w+31
     const int G = p.G;
     const int tl = row / G;
     const bool warp_rows = warp * 32 < p.G * p.QB;   // the warp holds a real row of some item
-    const float c2 = p.scale_log2;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bool ok = true;
     int g = 0;
     for (int k = 0; ok && k < n_mine; ++k) {
       const DtcItem t = item_of(k);
+      // raw logits -> base-2 exponents (FP8: the key scale of the item's head)
+      const float c2 = p.scale_log2 * (FP8 ? p.k_scale[t.kvh] : 1.f);
       const bool valid = tl < t.nq;
       const int pos = t.pos0 + tl;
       int lo_r = t.k_lo, hi_r = t.k_hi - 1;
@@ -474,8 +605,13 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
             const float a0 = ex2(fmaf(v[c][e], c2, -mb));
             const float a1 = ex2(fmaf(v[c][e + 1], c2, -mb));
             rs4[(e >> 1) & 3] += a0 + a1;
-            pk[e >> 1] = pack_bf16x2(a0, a1);
-            rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+            if constexpr (FP8) {
+              pk[e >> 1] = pack_f16x2(a0, a1);
+              rr4[(e >> 1) & 3] += f16x2_sum(pk[e >> 1]);
+            } else {
+              pk[e >> 1] = pack_bf16x2(a0, a1);
+              rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
+            }
           }
           // P columns [16c, 16c + 16) hold scores this thread already loaded
           tc::tmem_st16(s_addr + 16 * c, pk);
@@ -522,6 +658,8 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
       tc::fence_after_sync();
       const float4 mlr = ml[(k & 1) * 128 + row];
       const uint32_t o_addr = lane_base + C::COL_O + static_cast<uint32_t>((k & 1) * D);
+      const float vscale = FP8 ? p.v_scale[t.kvh] : 1.f;   // accumulator -> value units
+      const float lscale = FP8 ? p.sm_scale * p.k_scale[t.kvh] : p.sm_scale;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
@@ -536,7 +674,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(stage + row * C::XS + c * 32 + e) =
-                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                make_float4(o[e] * vscale, o[e + 1] * vscale, o[e + 2] * vscale, o[e + 3] * vscale);
         }
       }
       tc::fence_before_sync();
@@ -549,7 +687,7 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
         if (mlr.x == NEG_INF || !(mlr.z > 0.f)) {
           md = make_float2(NEG_INF, 0.f);
         } else {
-          md.x = mlr.x * p.sm_scale + (lg2(mlr.y) - lg2(mlr.z)) * kLn2;
+          md.x = mlr.x * lscale + (lg2(mlr.y) - lg2(mlr.z)) * kLn2;
           md.y = mlr.z;
         }
         *reinterpret_cast<float2*>(p.part_md + (rowid * S + t.split) * 2) = md;
@@ -575,27 +713,31 @@ __global__ void __launch_bounds__(DtcCfg<RR>::THREADS, 1)
   __syncthreads();
   // this CTA's partials are written: a dependent merge may start launching
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (warp == 11) {
+  if (warp == C::W_MMA) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------------------
-template <int RR, bool PAGED>
+template <int RR, bool PAGED, bool FP8 = false>
 static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
-  using C = DtcCfg<RR>;
+  using C = DtcCfg<RR, FP8>;
   const int G = a.Hq / a.Hkv;
   CUtensorMap tmQ, tmK, tmV;
   int rc = make_q_tmap(&tmQ, a.q, static_cast<uint64_t>(a.batch) * a.q_len, a.Hq, C::D, G, QB);
   if (rc) return rc;
   const uint64_t rows = kv_map_rows(a);
   const int box = kv_box_rows(a, C::KT);
-  rc = make_rows_tmap(&tmK, a.k, rows, C::D, box, 128);
+  rc = FP8 ? make_rows_tmap_u8(&tmK, a.k, rows, C::D, box)
+           : make_rows_tmap(&tmK, a.k, rows, C::D, box, 128);
   if (rc) return rc;
-  rc = make_rows_tmap(&tmV, a.v, rows, C::D, box, 128);
+  rc = FP8 ? make_rows_tmap_u8(&tmV, a.v, rows, C::D, box)
+           : make_rows_tmap(&tmV, a.v, rows, C::D, box, 128);
   if (rc) return rc;
   DtcParams p{};
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   p.page_size = a.page_size;
   p.box_rows = box;
   p.page_indptr = a.page_indptr;
@@ -622,7 +764,7 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
   p.window = a.window;
   p.part_acc = a.part_acc;
   p.part_md = a.part_md;
-  auto kern = decode_tc_kernel<RR, PAGED>;
+  auto kern = decode_tc_kernel<RR, PAGED, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -641,6 +783,8 @@ static int launch_dtc(const AttnArgs& a, int QB, cudaStream_t stream) {
 
 bool decode_tc_supported(const AttnArgs& a) {
   const int G = a.Hq / a.Hkv;
+  // FP8 (contiguous KV only): tiles of at most 64 rows, so the code ring fits
+  if (a.kv_fp8) return a.d == 128 && G >= 1 && G <= 64 && a.page_size == 0;
   return a.d == 128 && G >= 1 && G <= 128;
 }
 
@@ -649,6 +793,14 @@ int launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   if (!decode_tc_supported(a)) {
     set_error("the tcgen05 decode kernel needs head_dim 128 and at most 128 heads per group");
     return SINKATTN_UNSUPPORTED;
+  }
+  if (a.kv_fp8) {
+    const int QB = min(a.q_len, 64 / G);  // at most 64 rows per tile
+    const int R = G * QB;
+    if (R <= 16) return launch_dtc<16, false, true>(a, QB, stream);
+    if (R <= 32) return launch_dtc<32, false, true>(a, QB, stream);
+    if (R <= 48) return launch_dtc<48, false, true>(a, QB, stream);
+    return launch_dtc<64, false, true>(a, QB, stream);
   }
   const int QB = min(a.q_len, 128 / G);   // query tokens per CTA
   const int R = G * QB;                   // real rows of the 128-row tile

@@ -311,10 +311,11 @@ SINKATTN_API int sinkattn_decode_paged(const void* q, const void* k_pages, const
  * Sink attention", with the keys and values dequantised). The kernel widens
  * the codes to f16, which holds every e4m3 value exactly, and runs the
  * products in f16 with q converted to f16: |q| must stay below 65504, and
- * q elements below 2^-14 in magnitude lose relative precision. The partials
- * come from the warp-level kernel (SINKATTN_DECODE_TCGEN05 returns
- * SINKATTN_UNSUPPORTED). k_scale / v_scale null or misaligned:
- * SINKATTN_INVALID_ARG.
+ * q elements below 2^-14 in magnitude lose relative precision. Kernel
+ * choice (sinkattn_set_decode_kernel): at head_dim 128 with at most 64 query
+ * heads per KV head the tcgen05 kernel runs (AUTO or TCGEN05), other shapes
+ * take the warp-level kernel (TCGEN05 forced there: SINKATTN_UNSUPPORTED).
+ * k_scale / v_scale null or misaligned: SINKATTN_INVALID_ARG.
  */
 SINKATTN_API int sinkattn_decode_split_fp8(const void* q, const void* k, const void* v,
                                            const float* k_scale, const float* v_scale,

@@ -48,6 +48,7 @@ PAGED_DECODE_CASES = [
     (2, 16, 4, 1, 64, (16, 200), 2, 0, 64, 1.0),
     (2, 7, 32, 2, 128, (7, 600), 2, 33, 16, 1.0),      # 112 rows, window 33
     (3, 4, 64, 4, 128, (2000, 3000), 1, 0, 16, 1.0),   # long chunk over many 16-key pages
+    (2, 6, 32, 2, 128, (400, 900), 1, 0, 32, 1.0),     # 96 rows over many tiles: two-stage ring
 ]
 
 

@@ -179,6 +179,7 @@ DECODE_CASES = [
     (2, 1, 32, 2, 128, (1, 700), 3, 0),      # 16 rows per block (tcgen05 N = 16)
     (2, 2, 64, 4, 128, (2, 1500), 2, 64),    # 32 rows, window 64
     (1, 3, 64, 4, 128, (1900, 2100), 1, 0),  # one chunk of 16 tiles: 4 TMEM groups
+    (2, 8, 64, 4, 128, (600, 1500), 1, 0),   # 128 rows over many tiles: two-stage ring
 ]
 
 
