@@ -104,6 +104,9 @@ __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* c
   return t;
 }
 
+#ifndef SA_FP8_EXACT_L
+#define SA_FP8_EXACT_L 1
+#endif
 template <int RR, bool FP8 = false>
 struct DtcCfg {
   static constexpr int D = 128;
@@ -133,11 +136,14 @@ struct DtcCfg {
   static constexpr int N_BARS =
       2 + 2 + 2 * NST + 3 * NSB + 2 + 2 + 2 + 1 + (FP8 ? 2 * NSTF + 2 : 0);
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
-  // bf16: 12 warps (10 producer, 11 MMA); FP8: 14 warps, 8-11 convert, 12 producer, 13 MMA
-  static constexpr int THREADS = (FP8 ? 14 : 12) * 32;
-  static constexpr int W_PROD = FP8 ? 12 : 10;
-  static constexpr int W_MMA = FP8 ? 13 : 11;
+  // 12 warps. bf16: 0-3 softmax, 4-7 epilogue, 10 producer, 11 MMA. FP8 (at
+  // most 64 rows, so TMEM lane quarters 0 and 1): 0-1 softmax, 2-3 and 10-11
+  // convert (sub-partitions 2 and 3), 4-7 epilogue, 8 producer, 9 MMA.
+  static constexpr int THREADS = 12 * 32;
+  static constexpr int W_PROD = FP8 ? 8 : 10;
+  static constexpr int W_MMA = FP8 ? 9 : 11;
   static constexpr int N_CVT = 4;               // FP8 converter warps
+  static constexpr int N_SMX = FP8 ? 2 : 4;     // softmax warps
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = NSB * KT;   // O buffers at 256 and 384
   static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
@@ -176,12 +182,14 @@ struct DtcCfg {
 // applied -- the same state, rescaled, as (chunk max, exact sum).
 //
 // FP8 KV (e4m3 codes with per-KV-head scales): the producer copies the codes
-// into a ring of code stages; warps 8-11 (one per SM sub-partition) convert
-// each item's Q in place to f16 and widen each tile's codes to f16 into the
-// tile ring (the layout the MMAs read), and every MMA runs on f16 operands (P
-// is packed as f16). The producer moves to warp 12 and the MMA issuer to 13.
-// The key scale joins the item's logit scale, the value scale multiplies the
-// staged accumulator.
+// into a ring of code stages; warps 2-3 and 10-11 (the sub-partitions
+// without real softmax rows, as tiles have at most 64 rows) convert each
+// item's Q in place to f16 and widen each tile's codes to f16 into the tile
+// ring (the layout the MMAs read), and every MMA runs on f16 operands (P is
+// packed as f16). The producer moves to warp 8 and the MMA issuer to 9. The
+// key scale joins the item's logit scale, the value scale multiplies the
+// staged accumulator. Rows are normalised by the exact weight sum: f16
+// weights are within 2^-11 of it.
 template <int RR, bool PAGED, bool FP8>
 __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 4; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 32 * C::N_SMX);
       mbar_init(&pv_done[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
       mbar_init(&q_empty[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], 128);
-      mbar_init(&ml_full[i], 128);
+      mbar_init(&ml_full[i], 32 * C::N_SMX);
     }
     for (int i = 0; i < NST; ++i) {
       mbar_init(&kv_full[i], FP8 ? C::N_CVT : 1);   // FP8: the converter warps
@@ -462,13 +470,13 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
     if (leader) tc::commit(drain);
     __syncwarp();
     mbar_drain(drain, 0);
-  } else if (FP8 && warp >= 8 && warp < 8 + C::N_CVT) {
+  } else if (FP8 && (warp == 2 || warp == 3 || warp == 10 || warp == 11)) {
     // ------------------------------------------------------------ converters
     // Per item: its Q in place, bf16 -> f16 (same swizzled positions); per
     // tile: 16-byte chunks of e4m3 codes -> f16 into the tile ring stage.
     // Generic-proxy writes the tensor core reads: fenced before each hand-over.
     constexpr int NT = C::N_CVT * 32;
-    const int ct = static_cast<int>(threadIdx.x) - 8 * 32;   // 0 .. NT - 1
+    const int ct = ((warp < 4 ? warp - 2 : warp - 8) << 5) + lane;   // 0 .. NT - 1
     constexpr int CH_ROW = D / 16;          // 16-byte chunks per row of codes
     constexpr int CH_TILE = KT * CH_ROW;
     int g = 0, qi = 0;
@@ -607,7 +615,9 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
             rs4[(e >> 1) & 3] += a0 + a1;
             if constexpr (FP8) {
               pk[e >> 1] = pack_f16x2(a0, a1);
+#if !SA_FP8_EXACT_L
               rr4[(e >> 1) & 3] += f16x2_sum(pk[e >> 1]);
+#endif
             } else {
               pk[e >> 1] = pack_bf16x2(a0, a1);
               rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
@@ -632,6 +642,9 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
         }
         tc::tmem_wait_st();
         l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+#if SA_FP8_EXACT_L
+        if constexpr (FP8) lr = l; else
+#endif
         lr = lr * alpha + ((rr4[0] + rr4[1]) + (rr4[2] + rr4[3]));
         tc::fence_before_sync();
         mbar_arrive(&p_full[g & 3]);
