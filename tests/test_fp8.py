@@ -46,6 +46,8 @@ FP8_CASES = [
     (4, 1, 16, 16, 128, (1, 3000), 4, 0, 1.0),     # MHA: one row per item
     (2, 2, 128, 2, 128, (2, 400), 2, 0, 1.0),      # 64 heads per group, one token per tile
     (2, 16, 64, 8, 128, (16, 2500), 6, 200, 1.0),  # 8 heads x 8 tokens, window 200
+    # many items per CTA, chunks of 0 to 3 tiles (items that end within the S look-ahead)
+    (64, 3, 64, 4, 128, (100, 1200), 8, 0, 1.0),
 ]
 
 
