@@ -414,6 +414,14 @@ def decode_kernel_name(w):
     return "decode_tc_kernel (tcgen05)" if w.head_dim == 128 else "attn_mma_kernel (mma.sync)"
 
 
+def decode_traffic(w):
+    """ncu DRAM bytes per launch of the split kernel for this decode workload,
+    from the committed summaries (None if absent or the sources changed)."""
+    if "decode_tc" in decode_kernel_name(w):
+        return ncu_traffic("decode_tc_kernel/" + w.name, ["decode_tc.cu", "common.cuh", "tc.cuh"])
+    return ncu_traffic("attn_mma_kernel/" + w.name, ["attn_mma.cu", "common.cuh"])
+
+
 def _workload_desc(w):
     if w.kind == "decode":
         layout = ("paged HND bf16, %d-key pages in random order" % w.page_size if w.page_size > 0
@@ -508,7 +516,8 @@ def main():
                              "unit": "GB/s", "ms_per_step": ms_a,
                              "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
                              "num_splits": splits_of(wa, inp_a),
-                             "kernel": decode_kernel_name(wa) + " + merge_kernel"})
+                             "kernel": decode_kernel_name(wa) + " + merge_kernel",
+                             "traffic": decode_traffic(wa)})
             else:
                 tf = fl / (ms_a * 1e-3) / 1e12
                 also.append({"workload": _workload_desc(wa), "value": tf, "unit": "TFLOP/s",
