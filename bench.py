@@ -525,7 +525,8 @@ def main():
                              "peak_bf16_tflops": peaks["bf16_tflops"],
                              "hbm_gbs": nb / (ms_a * 1e-3) / 1e9,
                              "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "kernel": "prefill_tc_kernel (tcgen05)",
+                             "kernel": "prefill_tc_kernel or prefill_tc_persistent_kernel (tcgen05; "
+                                       "the library's launch choice)",
                              "traffic": ncu_traffic("prefill_tc_kernel/" + name,
                                                     ["prefill_tc.cu", "common.cuh", "tc.cuh"])})
             del inp_a
