@@ -71,12 +71,16 @@ struct DtcItem {
 
 // cu_k is read from `cu` (a shared-memory copy when the batch fits, else
 // global memory): every role derives every item's keys from it.
-template <int KT, bool PAGED>
+template <int KT, bool PAGED, bool ROTATE>
 __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* cu, int it) {
   DtcItem t;
   const int S = p.num_splits;
-  t.split = it % S;
   int r = it / S;
+  // ROTATE: the chunk index rotates with the group, so the CTAs that take
+  // every gridDim.x-th item see every chunk position (late chunks are often
+  // short or empty: a fixed position per CTA leaves some CTAs idle). Measured
+  // +4% on the bf16 MTP decode, -4% with FP8 KV (bound by per-tile work).
+  t.split = ROTATE ? (it % S + r) % S : it % S;
   const int qb = p.nqb - 1 - r % p.nqb;   // longer query blocks first
   r /= p.nqb;
   t.kvh = r % p.Hkv;
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
     for (int i = threadIdx.x; i < n_cu; i += blockDim.x) cu_s[i] = p.cu_k[i];
   const int32_t* cu = cu_in_smem ? cu_s : p.cu_k;
   auto item_of = [&](int k) {
-    return dtc_item<KT, PAGED>(p, cu, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x));
+    return dtc_item<KT, PAGED, !FP8>(p, cu, static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x));
   };
 
   if (threadIdx.x == 0) {
