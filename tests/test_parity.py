@@ -180,6 +180,7 @@ DECODE_CASES = [
     (2, 2, 64, 4, 128, (2, 1500), 2, 64),    # 32 rows, window 64
     (1, 3, 64, 4, 128, (1900, 2100), 1, 0),  # one chunk of 16 tiles: 4 TMEM groups
     (2, 8, 64, 4, 128, (600, 1500), 1, 0),   # 128 rows over many tiles: two-stage ring
+    (64, 3, 64, 4, 128, (100, 1200), 8, 0),  # many items per CTA, chunks of 0-3 tiles
 ]
 
 

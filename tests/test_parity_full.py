@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name", ["gptoss_decode", "qwen_mtp_decode", "gptoss_prefill",
                                   "gptoss_prefill_w128", "qwen_prefill", "gptoss_decode_paged",
-                                  "qwen_mtp_decode_paged"])
+                                  "qwen_mtp_decode_paged", "gptoss_decode_fp8",
+                                  "qwen_mtp_decode_fp8"])
 def test_full_size_sampled_rows(name):
     from gqa_attention_softmax_gb300 import _build
     _build.build()
@@ -36,11 +37,16 @@ def test_full_size_sampled_rows(name):
     B = inp["batch"]
     rng = np.random.default_rng(7)
     seqs = list(range(B)) if B <= 4 else sorted({0, B - 1, *rng.choice(B, 4, replace=False).tolist()})
-    sub = sub_problem(inp, Hkv, d, seqs)
+    scales = {}
+    if w.kv_fp8:   # the oracle reads the same e4m3 codes and per-KV-head scales
+        sub = sub_problem(dict(inp, k=inp["k_fp8"], v=inp["v_fp8"]), Hkv, d, seqs)
+        scales = dict(k_scale=inp["k_scale"].cpu(), v_scale=inp["v_scale"].cpu())
+    else:
+        sub = sub_problem(inp, Hkv, d, seqs)
     _, rows = sampled_rows(sub, Hq, 384, seed=3)
     want_out, want_lse = oracle.attend(sub["q"], sub["k"], sub["v"], sub["sinks"], sub["cu_q"],
                                        sub["cu_k"], Hq, Hkv, d, w.scale, w.causal, w.window,
-                                       rows=rows)
+                                       rows=rows, **scales)
     orig = sub["tok_map"][rows // Hq] * Hq + rows % Hq
     got_out = out.view(-1, d)[torch.from_numpy(orig).cuda()]
     got_lse = lse.view(-1)[torch.from_numpy(orig).cuda()]
