@@ -63,30 +63,35 @@ struct TcParams {
   const int32_t* page_indices;
 };
 
-template <int D, int NST>
+template <int D, int NST, int NT = 2>
 struct TcCfg {
-  // d 64: four S buffers shared round-robin by the two tiles, so S is issued
-  // three steps ahead of the P.V that frees its buffer and the tensor core
-  // always has queued work; d 128: one S buffer per tile (no room for more).
-  static constexpr bool RING = (D == 64);
+  // NT query tiles per CTA (one softmax warpgroup each). Two tiles at d 64:
+  // four S buffers shared round-robin, so S is issued three steps ahead of
+  // the P.V that frees its buffer and the tensor core always has queued
+  // work. Otherwise one S buffer per tile (three tiles at d 64, two at d 128:
+  // TMEM holds no more).
+  static constexpr bool RING = (D == 64 && NT == 2);
   static constexpr int NO = D;                    // O_t columns
   static constexpr int NSUB = D / 64;
-  static constexpr int KT = RING ? 96 : 128;      // keys per KV tile
-  static constexpr int NSB = RING ? 4 : 2;        // S buffers
+  static constexpr int KT = D == 64 ? 96 : 128;   // keys per KV tile
+  static constexpr int NSB = RING ? 4 : NT;       // S buffers
   static constexpr int QSUB = 128 * 128;          // [128 rows][64 bf16], 128B-swizzled: 16 KB
   static constexpr int KVSUB = KT * 128;          // [KT rows][64 bf16], 128B-swizzled
   static constexpr int Q_TILE = NSUB * QSUB;
   static constexpr int KV_TILE = NSUB * KVSUB;
   static constexpr int STAGE = 2 * KV_TILE;       // K and V of one KV tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
+  static constexpr int OFF_KV = OFF_Q + NT * Q_TILE;
   static constexpr int LIST_CAP = 512;            // items per CTA in the snake list
   static constexpr int CUQ_CAP = 1025;            // sequences staged for the item scan
   static constexpr int OFF_LIST = OFF_KV + NST * STAGE;   // [LIST_CAP + 32 + CUQ_CAP] ints
   static constexpr int OFF_BAR = OFF_LIST + ((LIST_CAP + 32 + CUQ_CAP) * 4 + 15) / 16 * 16;
-  static constexpr int N_BARS = 2 + 2 * NST + NSB + 2 + 2 + NSB + 1;
+  static constexpr int N_BARS = 2 + 2 * NST + NSB + NT + NT + NSB + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
-  static constexpr int THREADS = 320;             // TMA, MMA, 2 tiles x 4 softmax warps
+  static constexpr int THREADS = (2 + 4 * NT) * 32;   // TMA, MMA, NT tiles x 4 softmax warps
+  // registers per thread: 14 warps put 4 on two SM sub-partitions, whose
+  // 16384 registers then allow 128 a thread (bounded by a 512-thread launch)
+  static constexpr int LB_THREADS = NT == 2 ? 320 : 512;
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S buffers (P in the first KT / 2 columns of its S) at KT b,
   // O_t after them.
@@ -97,19 +102,20 @@ struct TcCfg {
   // S buffer of tile t at KV tile j, and how many times it was filled before
   __host__ __device__ static constexpr int buf_of(int t, int j) { return RING ? (2 * j + t) % NSB : t; }
   __host__ __device__ static constexpr int use_of(int t, int j) { return RING ? (2 * j + t) / NSB : j; }
-  static_assert(NSB * KT + 2 * NO <= 512, "TMEM budget");
+  static_assert(NSB * KT + NT * NO <= 512, "TMEM budget");
+  static_assert(NT == 2 || (NT == 3 && D == 64), "tiles per CTA");
   static_assert(KVSUB % 1024 == 0 && KT % 32 == 0, "tile shape");
 };
 
 // One block per item: block (x, y, z) runs query block nqb - 1 - x of KV head
 // y of sequence z (longest query blocks launch first), the hardware deals the
 // blocks out to the SMs as they free up.
-template <int D, int NST>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int NST, int NT>
+__global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
-  using C = TcCfg<D, NST>;
+  using C = TcCfg<D, NST, NT>;
   constexpr int KT = C::KT;
 
   extern __shared__ uint8_t smem_raw[];
@@ -120,9 +126,9 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = q_full + 1;
   uint64_t* kv_empty = kv_full + NST;
   uint64_t* s_full = kv_empty + NST;   // [NSB]: S written into buffer b
-  uint64_t* p_full = s_full + C::NSB;  // [2]: P_t(j) written and O_t rescaled (128 arrivals)
-  uint64_t* pv_done = p_full + 2;      // [2]: PV_t(j) completed
-  uint64_t* drain = pv_done + 2;
+  uint64_t* p_full = s_full + C::NSB;  // [NT]: P_t(j) written and O_t rescaled (128 arrivals)
+  uint64_t* pv_done = p_full + NT;     // [NT]: PV_t(j) completed
+  uint64_t* drain = pv_done + NT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* status = &g_status_prefill_tc;
@@ -137,9 +143,9 @@ __global__ void __launch_bounds__(320, 1)
   const int Lq = p.cu_q[b + 1] - q_start;
   const int k_start = p.cu_k[b];
   const int Lk = p.cu_k[b + 1] - k_start;
-  const int q0 = qb * 2 * p.QB;   // first token of tile A
+  const int q0 = qb * NT * p.QB;  // first token of tile 0
   if (q0 >= Lq) return;           // uniform over the CTA, before any barrier or TMEM use
-  const int nq = min(2 * p.QB, Lq - q0);
+  const int nq = min(NT * p.QB, Lq - q0);
   if (threadIdx.x == 0 && (Lk < Lq || Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
 
   const int pos0 = Lk - Lq + q0;
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&kv_empty[i], 1);
     }
     for (int i = 0; i < C::NSB; ++i) mbar_init(&s_full[i], 1);
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < NT; ++t) {
       mbar_init(&p_full[t], 128);
       mbar_init(&pv_done[t], 1);
     }
@@ -187,10 +193,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const uint32_t q_bytes = static_cast<uint32_t>(2 * C::NSUB * 128 * p.G * p.QB);
+      const uint32_t q_bytes = static_cast<uint32_t>(NT * C::NSUB * 128 * p.G * p.QB);
       mbar_arrive_expect_tx(q_full, q_bytes);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+      for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int sub = 0; sub < C::NSUB; ++sub)
           tc::tma_load_3d(smem + C::OFF_Q + t * C::Q_TILE + sub * C::QSUB, &tmQ, sub * 64,
@@ -298,8 +304,8 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
       };
-      // Order, one buffer per tile: S_A(0) S_B(0), then per KV tile j and
-      // tile t: PV_t(j), then S_t(j+1) into the same buffer once PV_t(j) is
+      // Order, one buffer per tile: S_t(0) for every tile, then per KV tile j
+      // and tile t: PV_t(j), then S_t(j+1) into the same buffer once PV_t(j) is
       // done (the tensor core may not overwrite P before the MMA has read it).
       // Ring of four, with k = 2 j + t the step's rank: S(0) S(1) S(2), then
       // per step PV(k), then S(k + 3) into the buffer of PV(k - 1) once that
@@ -309,8 +315,7 @@ __global__ void __launch_bounds__(320, 1)
         ok = wwait1(&kv_full[0], 0);
         if (ok) {
           tc::fence_after_sync();
-          issue_s(0, 0);
-          issue_s(1, 0);
+          for (int t = 0; t < NT; ++t) issue_s(t, 0);
         }
         if (ok && C::RING && n > 1) {
           ok = wwait1(&kv_full[1 % NST], (1 / NST) & 1);
@@ -321,11 +326,11 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       for (int j = 0; ok && j < n; ++j) {
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NT; ++t) {
           if (!wwait1(&p_full[t], j & 1)) { ok = false; break; }
           tc::fence_after_sync();
           issue_pv(t, j);
-          if (t == 1) {
+          if (t == NT - 1) {
             if (leader) tc::commit(&kv_empty[j % NST]);
             __syncwarp();
           }
@@ -1104,15 +1109,20 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int D, int NST>
+// NT query tiles per CTA for the one-block launch; the persistent launch
+// always runs two.
+template <int D, int NST, int NT>
 static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
-  using C = TcCfg<D, NST>;
+  static_assert(NT >= 2, "tiles per CTA");
+  using C = TcCfg<D, NST, NT>;
+  using CP = TcCfg<D, NST, 2>;
   const int G = a.Hq / a.Hkv;
   CUtensorMap tmQ, tmK, tmV;
   const int QB = 128 / G;
   int rc = make_q_tmap(&tmQ, a.q, static_cast<uint64_t>(a.total_q), a.Hq, D, G, QB);
   if (rc) return rc;
   const uint64_t rows = kv_map_rows(a);
+  static_assert(C::KT == CP::KT, "both launches tile the keys alike");
   const int box = kv_box_rows(a, C::KT);
   rc = make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
@@ -1130,7 +1140,8 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.Hkv = a.Hkv;
   p.G = G;
   p.QB = QB;
-  p.nqb = (a.max_q + 2 * QB - 1) / (2 * QB);
+  const int tiles = persistent ? 2 : NT;   // query tiles per item
+  p.nqb = (a.max_q + tiles * QB - 1) / (tiles * QB);
   p.batch = a.batch;
   const int64_t items = static_cast<int64_t>(p.nqb) * a.Hkv * a.batch;
   if (items >= (int64_t{1} << 31)) {
@@ -1147,8 +1158,10 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
 
-  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST> : prefill_tc_kernel<D, NST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST> : prefill_tc_kernel<D, NST, NT>;
+  const int smem = persistent ? CP::SMEM : C::SMEM;
+  const int threads = persistent ? CP::THREADS : C::THREADS;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     return SINKATTN_CUDA_ERROR;
@@ -1157,7 +1170,7 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   const dim3 grid = persistent ? dim3(static_cast<unsigned>(std::min<int64_t>(items, sm_count())))
                                : dim3(static_cast<unsigned>(p.nqb), static_cast<unsigned>(a.Hkv),
                                       static_cast<unsigned>(a.batch));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmQ, tmK, tmV, p);
+  kern<<<grid, threads, smem, stream>>>(tmQ, tmK, tmV, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("prefill kernel launch: %s", cudaGetErrorString(e));
@@ -1188,11 +1201,11 @@ int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
   if (a.d == 64) {
     const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
                       (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<64, 4>::KT));
-    return launch_tc<64, 4>(a, pers, stream);
+    return launch_tc<64, 4, 3>(a, pers, stream);
   }
   const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
                     (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<128, 2>::KT));
-  return launch_tc<128, 2>(a, pers, stream);
+  return launch_tc<128, 2, 2>(a, pers, stream);
 }
 
 int read_status_prefill_tc(cudaStream_t s, int* status) {
