@@ -108,9 +108,6 @@ __device__ __forceinline__ DtcItem dtc_item(const DtcParams& p, const int32_t* c
   return t;
 }
 
-#ifndef SA_FP8_EXACT_L
-#define SA_FP8_EXACT_L 1
-#endif
 template <int RR, bool FP8 = false>
 struct DtcCfg {
   static constexpr int D = 128;
@@ -618,10 +615,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
             const float a1 = ex2(fmaf(v[c][e + 1], c2, -mb));
             rs4[(e >> 1) & 3] += a0 + a1;
             if constexpr (FP8) {
-              pk[e >> 1] = pack_f16x2(a0, a1);
-#if !SA_FP8_EXACT_L
-              rr4[(e >> 1) & 3] += f16x2_sum(pk[e >> 1]);
-#endif
+              pk[e >> 1] = pack_f16x2(a0, a1);   // (normalised by the exact sum)
             } else {
               pk[e >> 1] = pack_bf16x2(a0, a1);
               rr4[(e >> 1) & 3] += bf16x2_sum(pk[e >> 1]);
@@ -646,10 +640,8 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
         }
         tc::tmem_wait_st();
         l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-#if SA_FP8_EXACT_L
-        if constexpr (FP8) lr = l; else
-#endif
-        lr = lr * alpha + ((rr4[0] + rr4[1]) + (rr4[2] + rr4[3]));
+        if constexpr (FP8) lr = l;
+        else lr = lr * alpha + ((rr4[0] + rr4[1]) + (rr4[2] + rr4[3]));
         tc::fence_before_sync();
         mbar_arrive(&p_full[g & 3]);
       }
