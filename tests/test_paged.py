@@ -116,12 +116,14 @@ def test_paged_prefill_matches_oracle(case):
     compare(out, lse, want_out, want_lse, "paged prefill")
 
 
+@pytest.mark.parametrize("page_size", [32, 128])
 @pytest.mark.parametrize("kernel", ["auto", "warp"])
-def test_paged_decode_with_too_few_pages_records_bad_lengths(kernel):
+def test_paged_decode_with_too_few_pages_records_bad_lengths(kernel, page_size):
     """A sequence given fewer pages than its key count needs: the kernel
-    reads only pool pages and records SINKATTN_BAD_LENGTHS."""
-    inp = _decode_inputs(3, 1, 16, 1, 128, (100, 200), seed=5)
-    pg = workloads.to_paged(inp, 1, 32, seed=1)
+    reads only pool pages and records SINKATTN_BAD_LENGTHS (pages smaller
+    than a tile and pages holding whole tiles)."""
+    inp = _decode_inputs(3, 1, 16, 1, 128, (100, 200) if page_size < 64 else (300, 600), seed=5)
+    pg = workloads.to_paged(inp, 1, page_size, seed=1)
     # drop the last page of sequence 1
     ind = pg["page_indptr"].tolist()
     idx = pg["page_indices"].tolist()
