@@ -5,37 +5,34 @@
 // Blackwell", section "Prefillers": prefill is compute-intensive, thousands
 // of tokens processed at once). Per CTA:
 //
-//  * rows: two tiles (A, B) of 128 (query token, head-in-group) pairs of one
-//    KV head -- each tile is QB = 128/G consecutive tokens times the G query
+//  * rows: NT query tiles of 128 (query token, head-in-group) pairs of one KV
+//    head -- each tile is QB = 128/G consecutive tokens times the G query
 //    heads sharing that KV head -- so one K/V tile in shared memory serves
-//    both tiles and the whole GQA group, and the causal diagonal cuts only a
-//    few keys of the last KV tile;
-//  * warp 0: TMA producer (Q_A and Q_B once as 3-D boxes, then K/V tiles of
-//    128 keys into an NST-stage ring, right-aligned to the end of the key
-//    range so no copy reads past the last key needed);
+//    every tile and the whole GQA group, and the causal diagonal cuts only a
+//    few keys of the last KV tile. NT is 3 at head_dim 64 in the one-block
+//    launch, 2 otherwise;
+//  * warp 0: TMA producer (the Q tiles once as 3-D boxes, then K/V tiles of
+//    KT keys -- 96 at head_dim 64, 128 at 128 -- into an NST-stage ring,
+//    right-aligned to the end of the key range so no copy reads past the
+//    last key needed);
 //  * warp 1: allocates TMEM and issues every MMA from one elected lane (the
-//    warp runs the schedule uniformly), ping-ponging
-//    the two tiles so the tensor core works on one while the other's softmax
-//    runs:  S_A(0), S_B(0), then per KV tile j:
-//           PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-//    with every shared-memory descriptor prepared once, so a group of MMAs
-//    issues back to back;
-//    with S_t = Q_t K^T (M 128, N 128, K d; both operands in shared memory)
-//    and O_t += P_t V (M 128, N d, K 128; P_t read from TMEM, V from shared);
-//  * warps 2-5 / 6-9: softmax of tile A / B, one thread per row (= TMEM
+//    warp runs the schedule uniformly), with S_t = Q_t K^T (M 128, N KT,
+//    K d; both operands in shared memory) and O_t += P_t V (M 128, N d, K KT;
+//    P_t read from TMEM, V from shared memory). With one S buffer per tile
+//    the order is S_t(0) for every tile, then per KV tile j and tile t:
+//    PV_t(j), then S_t(j+1) once PV_t(j) has completed (S overwrites P), so
+//    the tiles' chains interleave on the tensor core. The two-tile
+//    persistent launch at head_dim 64 shares four S buffers round-robin and
+//    keeps S three steps ahead of P.V;
+//  * warps 2 + 4t .. 5 + 4t: softmax of tile t, one thread per row (= TMEM
 //    lane). The running max starts at the head's sink and the running sum at
 //    1 ("GPT-OSS on Day 0", section "Kernels for GPT-OSS / Sink attention").
-//    Each thread loads its row's 128 scores from TMEM in one batch, so the
+//    Each thread loads its row's KT scores from TMEM in one batch, so the
 //    row maximum and sums need no exchange between threads; P goes back as
-//    bf16 into the first 64 columns of the same TMEM region. O_t is rescaled
-//    in TMEM when a row's maximum grows; the previous PV_t has completed by
-//    then, because S_t(j) is only issued after it. Row sums are kept both
-//    exact (for lse) and over the bf16-rounded weights the MMA applies (for
-//    out). With
-//    d = 64 the second sum comes from the tensor core: the P.V MMA is 80
-//    columns wide, its extra 16 columns multiplying P by a shared-memory block
-//    of bf16 ones, so O_t's column 64 holds exactly the sum of the weights the
-//    MMA applied (TMEM has room for that only at d = 64).
+//    bf16 into the first KT/2 columns of the same S buffer. The running
+//    maximum is exact, so a row's largest weight is exactly 1 in bf16; O_t is
+//    rescaled in TMEM when a row maximum grows, and out is divided by the
+//    exact fp32 row sum.
 //
 // Every wait is bounded; on a timeout the CTA records SINKATTN_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
@@ -361,7 +358,7 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    // 8 warps: tile t = A/B; warp w may access TMEM lanes 32 (w % 4) ...
+    // 4 NT warps: tile t = (warp - 2) / 4; warp w may access TMEM lanes 32 (w % 4) ...
     const int t = (warp - 2) >> 2;
     const int quad = warp & 3;       // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
