@@ -4,36 +4,20 @@
 // "Decoders"), and with MTP drafts sharing a KV head (3 tokens x 16 query
 // heads = 48 rows per Qwen3 KV head) every streamed KV byte costs 48
 // multiply-adds -- more than the warp-level mma.sync path sustains at HBM
-// speed on GB300. Here both products run on tcgen05 with a 128-row tile, the
-// CTA's R = G x QB real rows in its first R lanes and the rest padding:
+// speed on GB300. Here both products run on tcgen05 with a 128-row tile, an
+// item's R = G x QB real rows in its first R lanes and the rest padding:
 //
 //   S = Q K^T   M 128 rows, N 64 keys, K 128 d   (both operands in shared memory)
 //   O += P V    M 128 rows, N 128 d,  K 64 keys (P from TMEM, V from shared memory)
 //
-// One CTA = (sequence b, KV head, query block, KV chunk), as the warp-level
-// split kernel, and it writes the same partials: the chunk's (m, d, acc)
-// WITHOUT the sink, which the merge folds in once ("GPT-OSS on Day 0",
-// section "Kernels for GPT-OSS / Sink attention").
-//
-//  * warps 0-3: softmax, one thread per row (= TMEM lane, so each warp may
-//    only touch its own 32-lane quadrant): all 64 scores of a KV tile in
-//    registers, so the row maximum and sum need no exchange between threads.
-//    P goes back as bf16 into the first 32 columns of the same TMEM buffer.
-//    O is rescaled in TMEM only when some row of the warp raised its maximum.
-//  * warp 4: TMA producer -- Q once (a 3-D box of QB tokens x G heads), then
-//    K/V tiles of 64 keys into an NST-stage ring, right-aligned to the end of
-//    the chunk so no copy reads past the last key the CTA needs.
-//  * warp 5: TMEM allocation and every MMA, from one thread. Two S buffers
-//    alternate, so S(j+1) is computed while the softmax works on S(j):
-//      S(0), S(1), then per tile j:  PV(j), [PV(j) done] S(j+2).
-//
-// The Q tile holds only R rows in shared memory; the MMA's other 128 - R
-// rows read whatever follows (the ring), which only reaches padding lanes.
-// TMEM: S0 | S1 | O = 64 + 64 + 128 of 256 columns, so two CTAs share an SM
-// (shared memory admits at most two, and exactly two up to 48 rows), one
-// streaming while the other is in its prologue or epilogue. The partial rows
-// are staged in the (then idle) ring and written with coalesced stores.
-// Every wait is bounded.
+// A work item is (sequence b, KV head, query block, KV chunk), as in the
+// warp-level split kernel, and it writes the same partials: the chunk's
+// (m, d, acc) WITHOUT the sink, which the merge folds in once ("GPT-OSS on
+// Day 0", section "Kernels for GPT-OSS / Sink attention"). One persistent
+// CTA per SM runs items back to back (warp roles, buffers and the schedule
+// are described at the kernel below). The Q tile holds only RR rows in
+// shared memory; the MMA's other 128 - RR rows read whatever follows, which
+// only reaches padding lanes. Every wait is bounded.
 #include <algorithm>
 
 #include "common.cuh"
