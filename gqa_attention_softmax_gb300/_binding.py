@@ -235,11 +235,14 @@ def sinkattn_decode_noalloc(q, k, v, kv_indptr, sinks, q_len, max_kv_len, num_kv
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((rows, Hq), dtype=torch.float32, device=q.device)
-    rc = lib().sinkattn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), batch,
-                                       int(q_len), int(max_kv_len), Hq, int(num_kv_heads), d,
-                                       _scale(sm_scale, d), int(bool(causal)), int(window),
-                                       int(num_splits), _ptr(sinks), _ptr(out), _ptr(lse),
-                                       _stream(q, stream))
+    # the library looks the scratch address up in the current device's
+    # context and rejects a stream of another device: make q's device current
+    with torch.cuda.device(q.device):
+        rc = lib().sinkattn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), batch,
+                                           int(q_len), int(max_kv_len), Hq, int(num_kv_heads), d,
+                                           _scale(sm_scale, d), int(bool(causal)), int(window),
+                                           int(num_splits), _ptr(sinks), _ptr(out), _ptr(lse),
+                                           _stream(q, stream))
     _check(rc)
     return out, lse
 

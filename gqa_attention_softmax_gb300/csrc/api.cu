@@ -28,17 +28,19 @@ void set_error(const char* fmt, ...) {
 }
 
 int sm_count() {
-  static int cached[64] = {0};
+  // host threads may call the library concurrently: entries are atomics (a
+  // racing first fill stores the same value twice)
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
   if (dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

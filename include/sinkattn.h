@@ -130,7 +130,10 @@ SINKATTN_API int sinkattn_decode_split(const void* q, const void* k, const void*
  * Split-KV decode / MTP, step 2: fold the num_splits partials of every
  * (row, head) with the sink counted exactly once: the running state starts at
  * m = s_h, d = 1 (m = -inf, d = 0 without a sink) and absorbs each chunk with
- * the rescale to the larger maximum; out = acc / d, lse = m + ln d.
+ * the rescale to the larger maximum; out = acc / d, lse = m + ln d ("GPT-OSS
+ * on Day 0", section "Kernels for GPT-OSS / Sink attention": the running max
+ * m and scale d of the online softmax, the max seeded with the sink and d
+ * with 1, the sink in the first block only when the sequence is split).
  *   part_acc/part_md as produced by sinkattn_decode_split; rows = batch*q_len;
  *   out [rows, Hq, d] bf16; lse [rows, Hq] fp32 or NULL.
  */
@@ -139,8 +142,11 @@ SINKATTN_API int sinkattn_merge(const float* part_acc, const float* part_md, con
                    void* out, float* lse, void* stream);
 
 /*
- * Split-KV decode / MTP in one call: sinkattn_decode_split then sinkattn_merge
- * on the same stream, with the partials in the caller's workspace (at least
+ * Split-KV decode / MTP in one call ("GPT-OSS on Day 0", section "Kernels for
+ * GPT-OSS / Sink attention": parallel over heads and KV length, the sink
+ * counted once; "Hosting Qwen on Blackwell", section "Decoders": MTP drafts,
+ * q_len > 1, attend causally to the cache): sinkattn_decode_split then
+ * sinkattn_merge on the same stream, with the partials in the caller's workspace (at least
  * sinkattn_decode_workspace_bytes() bytes, 256-byte aligned, device memory;
  * contents on entry do not matter). num_splits <= 0 selects
  * sinkattn_decode_default_splits().
@@ -186,11 +192,16 @@ SINKATTN_API int sinkattn_decode_fused(const void* q, const void* k, const void*
  * are rejected with SINKATTN_UNSUPPORTED before anything launches. The call
  * allocates nothing and frees nothing.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture. Every call shares the one array: calls whose kernels may overlap on
- * the GPU (different streams, or several host threads) race on it and must be
- * serialised by the caller. Nothing needs clearing between calls.
+ * Set-up: the first call in each CUDA context looks up the array's device
+ * address (with that context current) and caches it under the context's
+ * unique id; make that first call before any stream capture. A new context
+ * (after cudaDeviceReset, or a non-primary context made current by another
+ * runtime) gets its own lookup on its first call. `stream` must belong to the
+ * current device (SINKATTN_INVALID_ARG otherwise, nothing launched): the
+ * address is only valid on that device. Every call shares the one array:
+ * calls whose kernels may overlap on the GPU (different streams, or several
+ * host threads) race on it and must be serialised by the caller. Nothing
+ * needs clearing between calls.
  */
 SINKATTN_API int sinkattn_decode_noalloc(const void* q, const void* k, const void* v,
                                          const int32_t* kv_indptr, int32_t batch, int32_t q_len,
