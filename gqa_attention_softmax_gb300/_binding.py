@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             L.sinkattn_last_error.argtypes = []
             L.sinkattn_last_error.restype = ctypes.c_char_p
             L.sinkattn_debug_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+            L.sinkattn_debug_set_hooks.argtypes = [ctypes.c_longlong, ctypes.c_int]
             L.sinkattn_set_decode_kernel.argtypes = [ctypes.c_int]
             L.sinkattn_set_prefill_kernel.argtypes = [ctypes.c_int]
             L.sinkattn_decode_split_fp8.argtypes = [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32,
@@ -75,7 +76,8 @@ def lib() -> ctypes.CDLL:
             for name in ("sinkattn_prefill", "sinkattn_decode_split", "sinkattn_merge",
                          "sinkattn_decode", "sinkattn_decode_fused", "sinkattn_decode_noalloc",
                          "sinkattn_decode_workspace_bytes", "sinkattn_decode_default_splits",
-                         "sinkattn_debug_status", "sinkattn_set_decode_kernel",
+                         "sinkattn_debug_status", "sinkattn_debug_set_hooks",
+                         "sinkattn_set_decode_kernel",
                          "sinkattn_set_prefill_kernel", "sinkattn_decode_split_fp8",
                          "sinkattn_decode_fp8",
                          "sinkattn_prefill_paged", "sinkattn_decode_split_paged",
@@ -404,3 +406,9 @@ def sinkattn_debug_status(stream=None) -> int:
         _stream(torch.empty(0, device="cuda"), stream))
     _check(lib().sinkattn_debug_status(s, ctypes.byref(st)))
     return int(st.value)
+
+
+def sinkattn_debug_set_hooks(wait_limit_cycles: int = 0, skip_tile: int = -1) -> None:
+    """Test only: bounded-wait limit in SM clock cycles (0: the default) and
+    the KV tile the first thread block's producer leaves out (-1: none)."""
+    _check(lib().sinkattn_debug_set_hooks(int(wait_limit_cycles), int(skip_tile)))

@@ -606,4 +606,15 @@ int sinkattn_debug_status(void* stream, int* status) {
   return SINKATTN_OK;
 }
 
+int sinkattn_debug_set_hooks(long long wait_limit_cycles, int skip_tile) {
+  g_last_error[0] = '\0';
+  if (skip_tile < -1) return fail(SINKATTN_INVALID_ARG, "skip_tile must be -1 or a tile index");
+  if (set_hooks_attn_mma(wait_limit_cycles, skip_tile) ||
+      set_hooks_prefill_tc(wait_limit_cycles, skip_tile) ||
+      set_hooks_decode_tc(wait_limit_cycles, skip_tile))
+    return fail(SINKATTN_CUDA_ERROR, "setting the test hooks failed: %s",
+                cudaGetErrorString(cudaGetLastError()));
+  return SINKATTN_OK;
+}
+
 }  // extern "C"

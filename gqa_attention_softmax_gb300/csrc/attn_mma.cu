@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         pc.start(p.page_indices + e0, np, first / p.page_size, lane);
       }
       int issued = 0;
+      const int skip_tile = hook_skip_tile();
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % NST;
         const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
@@ -198,6 +199,10 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
           // e4m3 codes into the code ring; the converter warps fill `full`
           if (!__all_sync(members, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
             break;
+          if (i == skip_tile) {   // test hook: the waits for this tile run out
+            issued = i + 1;
+            continue;
+          }
           uint8_t* kc = f8 + st * C::F8_STAGE;
           uint8_t* vc = kc + C::F8_TILE;
           if (leader) mbar_arrive_expect_tx(&full[st], C::F8_STAGE);
@@ -220,6 +225,10 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         }
         if (!__all_sync(members, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
           break;
+        if (i == skip_tile) {   // test hook: the waits for this tile run out
+          issued = i + 1;
+          continue;
+        }
         uint8_t* kt = tiles + st * C::STAGE_BYTES;
         uint8_t* vt = kt + C::TILE_BYTES;
         if (leader) mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
@@ -247,10 +256,14 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         }
         issued = i + 1;
       }
-      if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
+      // Let every issued copy land before this warp exits: the kernel has no
+      // final block-wide barrier, and when a wait gives up (the abort flag
+      // may be set after this loop ends) the consumers leave without reading
+      // every tile. A copy the consumers read has long landed, so this costs
+      // nothing otherwise; a left-out tile's phase never completes (bounded).
+      if (leader)
         for (int i = max(0, issued - NST); i < issued; ++i)
           mbar_drain(&full[i % NST], static_cast<uint32_t>(i / NST) & 1u);
-      }
     }
   } else {
   // ------------------------------------------------------------------ consumers
@@ -748,6 +761,8 @@ int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
 int launch_attn_mma_fused(const AttnArgs& a, cudaStream_t stream) {
   return launch_attn_mma_t<true, false>(a, stream);
 }
+
+SINKATTN_DEFINE_SET_HOOKS(set_hooks_attn_mma)
 
 int read_status_attn_mma(cudaStream_t s, int* status) {
   int zero = 0;

@@ -18,6 +18,29 @@ namespace sinkattn {
 // the kernel's status word and unwinds.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// Failure-detection test hooks (sinkattn_debug_set_hooks), one copy per
+// translation unit: the limit every bounded wait uses, and the KV tile whose
+// copies the producer of the grid's first thread block leaves out (-1: none),
+// so that the waits for that tile run out and take the timeout path.
+static __device__ long long g_wait_limit_cycles = kWaitLimitCycles;
+static __device__ int g_skip_tile = -1;
+
+// Sets this translation unit's hooks (host; synchronous). limit <= 0 restores
+// the default.
+#define SINKATTN_DEFINE_SET_HOOKS(fn)                                                        \
+  int fn(long long limit, int skip) {                                                        \
+    if (limit <= 0) limit = kWaitLimitCycles;                                                \
+    if (cudaMemcpyToSymbol(g_wait_limit_cycles, &limit, sizeof limit) != cudaSuccess ||      \
+        cudaMemcpyToSymbol(g_skip_tile, &skip, sizeof skip) != cudaSuccess)                  \
+      return SINKATTN_CUDA_ERROR;                                                            \
+    return SINKATTN_OK;                                                                      \
+  }
+
+// The tile the calling thread block's producer leaves out (test hook).
+__device__ __forceinline__ int hook_skip_tile() {
+  return (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? g_skip_tile : -1;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -INFINITY;
@@ -61,16 +84,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete. Returns false
-// if the CTA-wide abort flag is (or becomes) set, or after kWaitLimitCycles;
-// in the latter case it sets the abort flag and records a timeout.
+// if the CTA-wide abort flag is (or becomes) set, or after the wait limit
+// (kWaitLimitCycles unless a test hook changed it); in the latter case it sets
+// the abort flag and records a timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
+  const long long limit = g_wait_limit_cycles;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicExch(status, SINKATTN_TIMEOUT);
       return false;
@@ -82,8 +107,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // are still in flight before a CTA exits.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
+  const long long limit = g_wait_limit_cycles;
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return;
+    if (clock64() - t0 > limit) return;
   }
 }
 

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
   auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
   };
+  int g_prod = 0, qi_prod = 0;   // producer: tiles and Q loads issued
 
   if (warp == C::W_PROD) {
     // ---------------------------------------------------------------- producer
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
       [[maybe_unused]] PageCursor pc;
       int g = 0, qi = 0;                               // tile and non-empty item ordinals
       bool ok = true;
+      const int skip_tile = hook_skip_tile();
       for (int k = 0; ok && k < n_mine; ++k) {
         const DtcItem t = item_of(k);
         if (leader && (t.Lk < p.q_len || t.Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
             // the tile's e4m3 codes into the code ring (the converters fill the tile ring)
             const int sc = g % C::NSTF_MOD;
             if (!pwait(&c_empty[sc], ((g / C::NSTF_MOD) & 1) ^ 1)) { ok = false; break; }
+            if (g == skip_tile) continue;   // test hook: the waits for this tile run out
             uint8_t* codes = smem + C::OFF_CODE + sc * C::CODE_STAGE;
             if (leader) {
               mbar_arrive_expect_tx(&c_full[sc], C::CODE_STAGE);
@@ -317,6 +320,7 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
           }
           const int st = g % NST;
           if (!pwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
+          if (g == skip_tile) continue;   // test hook: the waits for this tile run out
           uint8_t* kt = smem + C::OFF_RING + st * C::STAGE;
           if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
           if constexpr (!PAGED) {
@@ -347,15 +351,8 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
           }
         }
       }
-      if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
-        for (int i = max(0, qi - 2); i < qi; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
-        if constexpr (FP8) {
-          for (int i = max(0, g - C::NSTF_MOD); i < g; ++i)
-            mbar_drain(&c_full[i % C::NSTF_MOD], (i / C::NSTF_MOD) & 1);
-        } else {
-          for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
-        }
-      }
+      g_prod = g;
+      qi_prod = qi;
     }
   } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- MMA issuer
@@ -702,8 +699,23 @@ __global__ void __launch_bounds__(DtcCfg<RR, FP8>::THREADS, 1)
     }
   }
 
+  // a warp that left its loop early may still have TMEM loads or stores in flight
+  tc::tmem_wait_ld();
+  tc::tmem_wait_st();
   tc::fence_before_sync();
   __syncthreads();
+  if (warp == C::W_PROD && lane == 0 && *abort_flag) {
+    // a wait gave up: let every issued copy land before the CTA's shared
+    // memory goes away (a left-out tile's phase never completes: bounded)
+    for (int i = max(0, qi_prod - 2); i < qi_prod; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
+    if constexpr (FP8) {
+      for (int i = max(0, g_prod - C::NSTF_MOD); i < g_prod; ++i)
+        mbar_drain(&c_full[i % C::NSTF_MOD], (i / C::NSTF_MOD) & 1);
+    } else {
+      for (int i = max(0, g_prod - NST); i < g_prod; ++i)
+        mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+    }
+  }
   // this CTA's partials are written: a dependent merge may start launching
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == C::W_MMA) {
@@ -810,6 +822,8 @@ int launch_decode_tc(const AttnArgs& a, cudaStream_t stream) {
   if (R <= 64) return launch_dtc<64, false>(a, QB, stream);
   return launch_dtc<128, false>(a, QB, stream);
 }
+
+SINKATTN_DEFINE_SET_HOOKS(set_hooks_decode_tc)
 
 int read_status_decode_tc(cudaStream_t s, int* status) {
   int zero = 0;

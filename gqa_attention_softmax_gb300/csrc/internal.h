@@ -101,6 +101,13 @@ int read_status_merge(cudaStream_t s, int* status);
 int read_status_prefill_tc(cudaStream_t s, int* status);
 int read_status_decode_tc(cudaStream_t s, int* status);
 
+// Failure-detection test hooks of one translation unit (wait limit in clock
+// cycles, <= 0: the default; KV tile the first thread block's producer leaves
+// out, -1: none). Host, synchronous.
+int set_hooks_attn_mma(long long limit, int skip);
+int set_hooks_prefill_tc(long long limit, int skip);
+int set_hooks_decode_tc(long long limit, int skip);
+
 // Thread-local error text used by the C ABI.
 void set_error(const char* fmt, ...);
 

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  int issued = 0;   // producer: KV tiles whose copies were issued (or left out by the test hook)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -208,11 +209,15 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
       if (leader && Lk > np * p.page_size) atomicExch(status, SINKATTN_BAD_LENGTHS);
       pc.start(p.page_indices + e0, np, first / p.page_size, lane);
     }
-    int issued = 0;
+    const int skip_tile = hook_skip_tile();
     for (int i = 0; i < n; ++i) {
       const int st = i % NST;
       if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1, abort_flag, status)))
         break;
+      if (i == skip_tile) {   // test hook: the waits for this tile run out
+        issued = i + 1;
+        continue;
+      }
       uint8_t* kt = smem + C::OFF_KV + st * C::STAGE;
       if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
       const int j0 = first + i * KT;
@@ -243,11 +248,6 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
         }
       }
       issued = i + 1;
-    }
-    if (leader && *abort_flag) {
-      mbar_drain(q_full, 0);
-      for (int i = max(0, issued - NST); i < issued; ++i)
-        mbar_drain(&kv_full[i % NST], (i / NST) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -529,8 +529,17 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
           l > 0.f ? (m_used * c2 + lg2(l)) * kLn2 : kNegInf;
   }
 
+  // a warp that left its loop early may still have TMEM loads or stores in flight
+  tc::tmem_wait_ld();
+  tc::tmem_wait_st();
   tc::fence_before_sync();
   __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // a wait gave up: let every issued copy land before the CTA's shared
+    // memory goes away (a left-out tile's phase never completes: bounded)
+    mbar_drain(q_full, 0);
+    for (int i = max(0, issued - NST); i < issued; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
@@ -699,6 +708,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  int g_prod = 0, qi_prod = 0;   // producer: KV tiles and Q loads issued
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -717,6 +727,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t q_bytes = static_cast<uint32_t>(2 * C::NSUB * 128 * p.G * p.QB);
     int g = 0, qi = 0;   // KV tiles and active items so far
     bool ok = true;
+    const int skip_tile = hook_skip_tile();
     for (int k = 0; ok && k < n_mine; ++k) {
       const PfItem t = pf_item<KT>(p, item_of(k));
       if (t.n < 0) continue;
@@ -744,6 +755,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; i < t.n; ++i, ++g) {
         const int st = g % NST;
         if (!pwait(&kv_empty[st], ((g / NST) & 1) ^ 1)) { ok = false; break; }
+        if (g == skip_tile) continue;   // test hook: the waits for this tile run out
         uint8_t* kt = smem + C::OFF_KV + st * C::STAGE;
         if (leader) mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
         const int j0 = t.first + i * KT;
@@ -777,10 +789,8 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-    if (leader && *abort_flag) {   // let every copy land before the CTA's shared memory goes away
-      if (qi > 0) mbar_drain(q_full, (qi - 1) & 1);
-      for (int i = max(0, g - NST); i < g; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
-    }
+    g_prod = g;
+    qi_prod = qi;
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     // The whole warp runs the schedule (waits and descriptor arithmetic stay
@@ -1097,8 +1107,17 @@ __global__ void __launch_bounds__(320, 1)
     }
   }
 
+  // a warp that left its loop early may still have TMEM loads or stores in flight
+  tc::tmem_wait_ld();
+  tc::tmem_wait_st();
   tc::fence_before_sync();
   __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // a wait gave up: let every issued copy land before the CTA's shared
+    // memory goes away (a left-out tile's phase never completes: bounded)
+    if (qi_prod > 0) mbar_drain(q_full, (qi_prod - 1) & 1);
+    for (int i = max(0, g_prod - NST); i < g_prod; ++i) mbar_drain(&kv_full[i % NST], (i / NST) & 1);
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
@@ -1204,6 +1223,8 @@ int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
                     (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<128, 2>::KT));
   return launch_tc<128, 2, 2>(a, pers, stream);
 }
+
+SINKATTN_DEFINE_SET_HOOKS(set_hooks_prefill_tc)
 
 int read_status_prefill_tc(cudaStream_t s, int* status) {
   int zero = 0;

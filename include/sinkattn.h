@@ -360,6 +360,21 @@ SINKATTN_API const char* sinkattn_last_error(void);
  */
 SINKATTN_API int sinkattn_debug_status(void* stream, int* status);
 
+/*
+ * Diagnostic, test only (failure detection without a GPU fault; the pages
+ * have no counterpart): sets, for every kernel of the library, the number of
+ * SM clock cycles a bounded wait allows before it gives up
+ * (wait_limit_cycles <= 0 restores the default, about 1 s), and makes the
+ * TMA producer of the first thread block of every later launch leave out the
+ * copies of its KV tile number skip_tile (-1: none). A left-out tile's
+ * waits run out: the kernel records SINKATTN_TIMEOUT (read by
+ * sinkattn_debug_status), drains its copies and MMAs, frees its tensor
+ * memory and exits; its outputs are then undefined. Host call, synchronous
+ * with the device; make it while no kernel of the library is running.
+ * skip_tile < -1: SINKATTN_INVALID_ARG.
+ */
+SINKATTN_API int sinkattn_debug_set_hooks(long long wait_limit_cycles, int skip_tile);
+
 #ifdef __cplusplus
 }
 #endif
