@@ -34,8 +34,13 @@ import torch  # noqa: E402
 
 HEADLINE = "gptoss_decode"
 ALSO = ["qwen_mtp_decode", "gptoss_prefill", "gptoss_prefill_w128", "qwen_prefill",
-        "gptoss_decode_paged", "qwen_mtp_decode_paged", "gptoss_decode_fp8",
+        "gptoss_mtp2_decode", "gptoss_mtp4_decode", "qwen_mtp2_decode", "qwen_mtp4_decode",
+        "qwen_mtp16_decode", "gptoss_decode_paged", "qwen_mtp_decode_paged", "gptoss_decode_fp8",
         "qwen_mtp_decode_fp8"]
+# secondary workloads that get the oracle timed beside them (the other named
+# configurations; the headline has its own cpu_baseline)
+CPU_ALSO = ("qwen_mtp_decode", "gptoss_prefill", "gptoss_prefill_w128", "qwen_prefill")
+ALSO_FIELDS = "value, unit, frac of measured peak, ms/step, oracle on host cores (same unit)"
 METRIC = "decode KV-read HBM GB/s and prefill TFLOP/s, each as % of GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2**20
@@ -232,6 +237,26 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
     return ms, split_ms, w, inp, run
 
 
+def time_flushed(run, steps, dist_ctx=None, flush_bytes=256 * 2**20):
+    """Device time of one pass with L2 flushed before it: a `flush_bytes`
+    write between passes, outside the events. Returns ms per pass (median)."""
+    stream = torch.cuda.current_stream()
+    buf = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
+    times = []
+    _sync(dist_ctx)
+    for _ in range(steps):
+        buf.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    _sync(dist_ctx)
+    del buf
+    return _max_over_ranks(statistics.median(times), dist_ctx)
+
+
 def _sync(ctx):
     torch.cuda.synchronize()
     if ctx is not None:
@@ -327,7 +352,7 @@ def oracle_sample(w, inp, target_s):
               "total_q": sum(cu_q[b + 1] - cu_q[b] for b in seqs), "batch": len(seqs)}
         nbytes, _, _ = work(w, wl)
         return (passes * nbytes / total / 1e9, "GB/s", oracle.num_threads(),
-                "%d pass(es) over %d of %d sequences (all heads, all rows), %.1f s" % (passes, len(seqs), B, total))
+                "%d passes over %d of %d seqs, all rows, %.1f s" % (passes, len(seqs), B, total))
     # prefill: random rows, flops counted per row
     n = 64
     while True:
@@ -349,7 +374,7 @@ def oracle_sample(w, inp, target_s):
         hi = p if w.causal else lk - 1
         lo = max(0, p - w.window + 1) if w.window > 0 else 0
         pairs += max(0, hi - lo + 1)
-    return 4.0 * d * pairs / dt / 1e12, "TFLOP/s", oracle.num_threads(), "%d random (row, head) pairs, %.1f s" % (n, dt)
+    return 4.0 * d * pairs / dt / 1e12, "TFLOP/s", oracle.num_threads(), "%d random rows, %.1f s" % (n, dt)
 
 
 def _sub(inp, Hkv, seqs, cu_q, cu_k):
@@ -501,18 +526,20 @@ def main():
         split_bytes = nbytes
         kernel_name = "attn_mma_kernel, cluster-fused split-KV decode (%d chunks per cluster)" % run.num_splits
     else:
-        kernel_name = decode_kernel_name(w) + " (split-KV partials, then merge_kernel)"
+        kernel_name = decode_kernel_name(w).split(" ")[0]
     split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
     traffic = ncu_traffic(("attn_mma_kernel_fused/" if run.fused else "attn_mma_kernel/") + HEADLINE,
                           ["attn_mma.cu", "common.cuh"])
 
+    flushed_ms = time_flushed(run, max(3, min(args.steps, 50)), dist_ctx)
+
     e2e = None
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_decode(w, inp, run, steps=min(args.steps, 20))
-        e2e = {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        e2e = {"value": _r(world * nbytes / (e2e_ms * 1e-3) / 1e9), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    also = []
+    also, detail = {}, {}
     if not args.no_also:
         for name in ALSO:
             wa = workloads.WORKLOADS[name]
@@ -520,24 +547,30 @@ def main():
             ms_a, split_a, wa, inp_a, _ = time_workload(name, steps, args.warmup, dist_ctx,
                                                         want_kernel_split=(wa.kind == "decode"))
             nb, fl, sb = work(wa, inp_a)
+            cpu_a = None
+            if rank == 0 and not args.no_cpu and name in CPU_ALSO:
+                inp_c = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp_a.items()}
+                cpu_a = oracle_sample(wa, inp_c, target_s=4.0)[0]
+                del inp_c
+            gbs = nb / (ms_a * 1e-3) / 1e9
             if wa.kind == "decode":
-                also.append({"workload": _workload_desc(wa), "value": nb / (ms_a * 1e-3) / 1e9,
-                             "unit": "GB/s", "ms_per_step": ms_a,
-                             "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "num_splits": splits_of(wa, inp_a),
-                             "kernel": decode_kernel_name(wa) + " + merge_kernel",
-                             "traffic": decode_traffic(wa)})
+                also[name] = [_r(gbs), "GB/s", _r(gbs / peaks["hbm_gbs"], 3), _r(ms_a, 3), _r(cpu_a, 3)]
+                detail[name] = {"workload": _workload_desc(wa), "num_splits": splits_of(wa, inp_a),
+                                "kernel": decode_kernel_name(wa) + " + merge_kernel",
+                                "split_kernel_ms": _r(split_a),
+                                "traffic": decode_traffic(wa), "tflops": _r(fl / (ms_a * 1e-3) / 1e12)}
             else:
                 tf = fl / (ms_a * 1e-3) / 1e12
-                also.append({"workload": _workload_desc(wa), "value": tf, "unit": "TFLOP/s",
-                             "ms_per_step": ms_a, "frac_of_bf16": tf / peaks["bf16_tflops"],
-                             "peak_bf16_tflops": peaks["bf16_tflops"],
-                             "hbm_gbs": nb / (ms_a * 1e-3) / 1e9,
-                             "frac_of_hbm": nb / (ms_a * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "kernel": "prefill_tc_kernel or prefill_tc_persistent_kernel (tcgen05; "
-                                       "the library's launch choice)",
-                             "traffic": ncu_traffic("prefill_tc_kernel/" + name,
-                                                    ["prefill_tc.cu", "common.cuh", "tc.cuh"])})
+                also[name] = [_r(tf), "TFLOP/s", _r(tf / peaks["bf16_tflops"], 3), _r(ms_a, 3),
+                              _r(cpu_a, 3)]
+                if wa.window > 0:   # the HBM roofline binds (arithmetic intensity below the ridge)
+                    also[name + "_hbm"] = [_r(gbs), "GB/s", _r(gbs / peaks["hbm_gbs"], 3),
+                                           _r(ms_a, 3), None]
+                detail[name] = {"workload": _workload_desc(wa),
+                                "kernel": "prefill_tc_kernel or prefill_tc_persistent_kernel "
+                                          "(tcgen05; the library's launch choice)",
+                                "traffic": ncu_traffic("prefill_tc_kernel/" + name,
+                                                       ["prefill_tc.cu", "common.cuh", "tc.cuh"])}
             del inp_a
             torch.cuda.empty_cache()
 
@@ -545,32 +578,45 @@ def main():
     if rank == 0 and not args.no_cpu:
         inp_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
         v_cpu, unit, cores, sample = oracle_sample(w, inp_cpu, target_s=10.0)
-        cpu = {"value": v_cpu, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = {"value": _r(v_cpu), "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
+        if detail:
+            # kernel names, splits and ncu traffic of the secondary workloads
+            print(json.dumps({"detail": detail}), flush=True)
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "metric": METRIC, "value": _r(value), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": _r(ms),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
             "config": {"workload": _workload_desc(w), "num_splits": run.num_splits,
-                       "l2": "inputs larger than L2 (%.0f MB of K/V per step vs 129 MB L2), no flush" % (split_bytes / 1e6),
+                       "l2": "inputs > L2 (%.0f MB K/V per step); l2_flushed: 256 MB written "
+                             "before each pass" % (split_bytes / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "kernel": kernel_name,
-                         "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": split_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                         "algorithmic_bytes_per_launch": split_bytes,
-                         "peak_source": "%s (hbm_gbs)" % peak_src},
-            "step_frac_of_hbm": value / world / peaks["hbm_gbs"],
+                         "achieved": _r(split_gbs), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": _r(split_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                         "bytes_per_launch": split_bytes, "peak_source": peak_src},
+            "l2_flushed": {"value": _r(world * nbytes / (flushed_ms * 1e-3) / 1e9),
+                           "ms_per_step": _r(flushed_ms)},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": run.launches_per_call * args.steps,
             "clocks": clocks,
+            "also_fields": ALSO_FIELDS,
             "also": also,
         }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if dist_ctx is not None:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def _r(x, digits=4):
+    """x to `digits` significant digits (None stays None): keeps the JSON line short."""
+    if x is None:
+        return None
+    return float("%.*g" % (digits, x))
 
 
 def splits_of(w, inp):

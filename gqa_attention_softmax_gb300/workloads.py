@@ -87,6 +87,23 @@ WORKLOADS = {
     # Qwen3-235B-shaped MTP speculative decode: 3 drafts, 16 KV chunks.
     "qwen_mtp_decode": Workload("qwen_mtp_decode", "decode", 64, 4, 128, True, batch=256, q_len=3,
                                 kv_range=(4000, 8000), num_splits=16, sink_dist="uniform2"),
+    # Wider MTP / speculative drafts ("Hosting Qwen on Blackwell", section
+    # "Decoders"): 2 and 4 drafts at both layouts, 16 drafts at the Qwen one.
+    "gptoss_mtp2_decode": Workload("gptoss_mtp2_decode", "decode", 64, 8, 64, True, batch=64,
+                                   q_len=2, kv_range=(1024, 8192), sink_dist="uniform2",
+                                   sm_scale=1.0 / 8.0),
+    "gptoss_mtp4_decode": Workload("gptoss_mtp4_decode", "decode", 64, 8, 64, True, batch=64,
+                                   q_len=4, kv_range=(1024, 8192), sink_dist="uniform2",
+                                   sm_scale=1.0 / 8.0),
+    "qwen_mtp2_decode": Workload("qwen_mtp2_decode", "decode", 64, 4, 128, True, batch=256,
+                                 q_len=2, kv_range=(4000, 8000), num_splits=16,
+                                 sink_dist="uniform2"),
+    "qwen_mtp4_decode": Workload("qwen_mtp4_decode", "decode", 64, 4, 128, True, batch=256,
+                                 q_len=4, kv_range=(4000, 8000), num_splits=16,
+                                 sink_dist="uniform2"),
+    "qwen_mtp16_decode": Workload("qwen_mtp16_decode", "decode", 64, 4, 128, True, batch=256,
+                                  q_len=16, kv_range=(4000, 8000), num_splits=16,
+                                  sink_dist="uniform2"),
     # The two decodes over an FP8 (e4m3) KV cache with per-KV-head scales.
     "gptoss_decode_fp8": Workload("gptoss_decode_fp8", "decode", 64, 8, 64, True, batch=64,
                                   q_len=1, kv_range=(1024, 8192), sink_dist="uniform2",

@@ -181,6 +181,14 @@ DECODE_CASES = [
     (1, 3, 64, 4, 128, (1900, 2100), 1, 0),  # one chunk of 16 tiles: 4 TMEM groups
     (2, 8, 64, 4, 128, (600, 1500), 1, 0),   # 128 rows over many tiles: two-stage ring
     (64, 3, 64, 4, 128, (100, 1200), 8, 0),  # many items per CTA, chunks of 0-3 tiles
+    # MTP / speculative drafts at the gpt-oss layout (64/8, d 64) ...
+    (3, 2, 64, 8, 64, (2, 900), 4, 0),
+    (3, 3, 64, 8, 64, (3, 900), 4, 0),
+    (3, 4, 64, 8, 64, (4, 1200), 3, 0),
+    # ... and at the Qwen layout (64/4, d 128), up to 16 drafts (256 rows: two query blocks)
+    (3, 2, 64, 4, 128, (2, 1400), 16, 0),
+    (3, 4, 64, 4, 128, (4, 1400), 16, 0),
+    (2, 16, 64, 4, 128, (16, 900), 4, 0),
 ]
 
 

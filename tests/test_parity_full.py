@@ -17,7 +17,9 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("name", ["gptoss_decode", "qwen_mtp_decode", "gptoss_prefill",
                                   "gptoss_prefill_w128", "qwen_prefill", "gptoss_decode_paged",
                                   "qwen_mtp_decode_paged", "gptoss_decode_fp8",
-                                  "qwen_mtp_decode_fp8"])
+                                  "qwen_mtp_decode_fp8", "gptoss_mtp2_decode",
+                                  "gptoss_mtp4_decode", "qwen_mtp2_decode", "qwen_mtp4_decode",
+                                  "qwen_mtp16_decode"])
 def test_full_size_sampled_rows(name):
     from gqa_attention_softmax_gb300 import _build
     _build.build()
