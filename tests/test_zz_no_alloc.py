@@ -43,8 +43,14 @@ def test_noalloc_scratch_boundary_is_host_side():
     from gqa_attention_softmax_gb300 import _build
     _build.build()
     Hq, S, d = 4, 25, 64
-    per_seq = sa.sinkattn_decode_workspace_bytes(1, 1, Hq, d, S)
-    fit = SCRATCH_BYTES // per_seq
+    lo, hi = 1, 1 << 20   # the largest batch whose partials fit, by bisection
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if sa.sinkattn_decode_workspace_bytes(mid, 1, Hq, d, S) <= SCRATCH_BYTES:
+            lo = mid
+        else:
+            hi = mid
+    fit = lo
     assert sa.sinkattn_decode_workspace_bytes(fit, 1, Hq, d, S) <= SCRATCH_BYTES
     assert sa.sinkattn_decode_workspace_bytes(fit + 1, 1, Hq, d, S) > SCRATCH_BYTES
     rc = _raw_call(fit, 1, Hq, 1, d, S)
