@@ -199,7 +199,7 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
     e1.record(stream)
     _sync(dist_ctx)
     ms = e0.elapsed_time(e1) / steps
-    if w.kind == "decode" and want_kernel_split and not run.fused:
+    if w.kind == "decode" and want_kernel_split and not run.fused and not single_pass_decode(w):
         # the dominant kernel's own time: the same partial launches back to
         # back, bracketed by events on the launching stream
         n_acc = inp["total_q"] * w.num_qo_heads * run.num_splits * w.head_dim * 4
@@ -230,7 +230,7 @@ def time_workload(name, steps, warmup, dist_ctx=None, want_kernel_split=False, b
         _sync(dist_ctx)
         split_ms = s0.elapsed_time(s1) / steps
     elif w.kind == "decode":
-        split_ms = ms   # the fused kernel is the whole step
+        split_ms = ms   # one launch (cluster-fused, or single pass) is the whole step
     ms = _max_over_ranks(ms, dist_ctx)
     if split_ms is not None:
         split_ms = _max_over_ranks(split_ms, dist_ctx)
@@ -438,8 +438,16 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def single_pass_decode(w):
+    """True when the library's default runs this decode as one single-pass
+    launch: more query rows per KV head (G x q_len) than one 128-row tile."""
+    return not w.kv_fp8 and (w.num_qo_heads // w.num_kv_heads) * w.q_len > 128
+
+
 def decode_kernel_name(w):
-    """The split kernel the library's default selection runs for this shape."""
+    """The kernel the library's default selection runs for this shape."""
+    if single_pass_decode(w):
+        return "prefill_tc_kernel (tcgen05, single pass: the drafts are its queries)"
     if w.kv_fp8:
         g = w.num_qo_heads // w.num_kv_heads
         if w.head_dim == 128 and g <= 64:
@@ -556,7 +564,8 @@ def main():
             if wa.kind == "decode":
                 also[name] = [_r(gbs), "GB/s", _r(gbs / peaks["hbm_gbs"], 3), _r(ms_a, 3), _r(cpu_a, 3)]
                 detail[name] = {"workload": _workload_desc(wa), "num_splits": splits_of(wa, inp_a),
-                                "kernel": decode_kernel_name(wa) + " + merge_kernel",
+                                "kernel": decode_kernel_name(wa) + (
+                                    "" if single_pass_decode(wa) else " + merge_kernel"),
                                 "split_kernel_ms": _r(split_a),
                                 "traffic": decode_traffic(wa), "tflops": _r(fl / (ms_a * 1e-3) / 1e12)}
             else:

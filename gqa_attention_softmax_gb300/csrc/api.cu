@@ -393,6 +393,29 @@ int decode_impl(const void* q, const void* k, const void* v, const int32_t* kv_i
   if (!out || !aligned16(out)) return fail(SINKATTN_INVALID_ARG, "out must be non-null and 16-byte aligned");
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
     return fail(SINKATTN_INVALID_ARG, "lse must be 4-byte aligned");
+  // More query rows per KV head than one 128-row tile holds (G x q_len > 128,
+  // e.g. 16 MTP drafts of 16 heads): the split kernels would read every KV
+  // tile once per 128-row block; the single-pass prefill kernel (decode
+  // drafts are its queries, bottom-right causal) reads each once and needs
+  // no partials. Only under the default kernel choice, bf16 KV.
+  if (!f8 && batch > 0 && static_cast<int64_t>(num_qo_heads / num_kv_heads) * q_len > 128 &&
+      g_decode_kernel.load(std::memory_order_relaxed) == SINKATTN_DECODE_AUTO &&
+      (head_dim == 64 || head_dim == 128)) {
+    AttnArgs a;
+    rc = decode_args(q, k, v, kv_indptr, batch, q_len, max_kv_len, num_qo_heads, num_kv_heads,
+                     head_dim, sm_scale, causal, window, num_splits, &a);
+    if (rc) return rc;
+    if (pg && (rc = check_paged(*pg, num_kv_heads))) return rc;
+    if (static_cast<int64_t>(batch) * q_len >= (int64_t{1} << 31))
+      return fail(SINKATTN_UNSUPPORTED, "too many query rows");
+    set_paged(&a, pg);
+    a.total_q = batch * q_len;
+    a.sinks = sinks;
+    a.out = out;
+    a.lse = lse;
+    return launch_prefill_tc(a, g_prefill_kernel.load(std::memory_order_relaxed),
+                             static_cast<cudaStream_t>(stream));
+  }
   const size_t slots = static_cast<size_t>(batch) * q_len * num_qo_heads * num_splits;
   float* part_acc = static_cast<float*>(workspace);
   float* part_md = reinterpret_cast<float*>(static_cast<char*>(workspace) +

@@ -45,8 +45,9 @@ namespace sinkattn {
 __device__ int g_status_prefill_tc;
 
 struct TcParams {
-  const int32_t* cu_q;
+  const int32_t* cu_q;      // nullptr: every sequence has q_len queries (decode drafts)
   const int32_t* cu_k;
+  int q_len;
   int batch, n_items;
   int Hq, Hkv, G, QB, nqb, max_kv;
   float sm_scale, scale_log2;
@@ -136,8 +137,8 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
   const int kvh = blockIdx.y;
   const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x);   // longest query blocks first
 
-  const int q_start = p.cu_q[b];
-  const int Lq = p.cu_q[b + 1] - q_start;
+  const int q_start = p.cu_q ? p.cu_q[b] : b * p.q_len;
+  const int Lq = p.cu_q ? p.cu_q[b + 1] - q_start : p.q_len;
   const int k_start = p.cu_k[b];
   const int Lk = p.cu_k[b + 1] - k_start;
   const int q0 = qb * NT * p.QB;  // first token of tile 0
@@ -561,8 +562,8 @@ __device__ __forceinline__ PfItem pf_item(const TcParams& p, int it) {
   const int r = it % per;
   t.kvh = r % p.Hkv;
   t.b = r / p.Hkv;
-  t.q_start = p.cu_q[t.b];
-  t.Lq = p.cu_q[t.b + 1] - t.q_start;
+  t.q_start = p.cu_q ? p.cu_q[t.b] : t.b * p.q_len;
+  t.Lq = p.cu_q ? p.cu_q[t.b + 1] - t.q_start : p.q_len;
   t.k_start = p.cu_k[t.b];
   t.Lk = p.cu_k[t.b + 1] - t.k_start;
   t.q0 = qb * 2 * p.QB;   // first token of tile A
@@ -654,13 +655,13 @@ __global__ void __launch_bounds__(320, 1)
   const int G = static_cast<int>(gridDim.x);
   const bool staged = p.batch + 1 <= C::CUQ_CAP;
   if (staged)
-    for (int i = threadIdx.x; i <= p.batch; i += blockDim.x) cuq_s[i] = p.cu_q[i];
+    for (int i = threadIdx.x; i <= p.batch; i += blockDim.x) cuq_s[i] = p.cu_q ? p.cu_q[i] : i * p.q_len;
   __syncthreads();
   const int per = p.Hkv * p.batch;
   auto has_rows = [&](int it) -> bool {
     const int qb = p.nqb - 1 - it / per;
     const int b = (it % per) / p.Hkv;
-    const int Lq = staged ? cuq_s[b + 1] - cuq_s[b] : p.cu_q[b + 1] - p.cu_q[b];
+    const int Lq = staged ? cuq_s[b + 1] - cuq_s[b] : (p.cu_q ? p.cu_q[b + 1] - p.cu_q[b] : p.q_len);
     return qb * 2 * p.QB < Lq;
   };
   int n_list = 0, total = 0;
@@ -1152,6 +1153,7 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.page_indices = a.page_indices;
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
+  p.q_len = a.q_len;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.G = G;

@@ -149,7 +149,12 @@ SINKATTN_API int sinkattn_merge(const float* part_acc, const float* part_md, con
  * sinkattn_merge on the same stream, with the partials in the caller's workspace (at least
  * sinkattn_decode_workspace_bytes() bytes, 256-byte aligned, device memory;
  * contents on entry do not matter). num_splits <= 0 selects
- * sinkattn_decode_default_splits().
+ * sinkattn_decode_default_splits(). When a KV head has more query rows than
+ * one 128-row tile (G x q_len > 128, e.g. 16 drafts of 16 heads) and the
+ * kernel choice is SINKATTN_DECODE_AUTO, the call runs the single-pass
+ * prefill kernel instead (the drafts are its queries, bottom-right causal,
+ * every KV tile read once); the workspace is then unused and num_splits has
+ * no effect on the result.
  */
 SINKATTN_API int sinkattn_decode(const void* q, const void* k, const void* v, const int32_t* kv_indptr,
                     int32_t batch, int32_t q_len, int32_t max_kv_len, int32_t num_qo_heads,
