@@ -459,6 +459,8 @@ def decode_kernel_name(w):
 def decode_traffic(w):
     """ncu DRAM bytes per launch of the split kernel for this decode workload,
     from the committed summaries (None if absent or the sources changed)."""
+    if single_pass_decode(w):
+        return ncu_traffic("prefill_tc_kernel/" + w.name, ["prefill_tc.cu", "common.cuh", "tc.cuh"])
     if "decode_tc" in decode_kernel_name(w):
         return ncu_traffic("decode_tc_kernel/" + w.name, ["decode_tc.cu", "common.cuh", "tc.cuh"])
     return ncu_traffic("attn_mma_kernel/" + w.name, ["attn_mma.cu", "common.cuh"])
