@@ -81,7 +81,8 @@ int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int
   return SINKATTN_OK;
 }
 
-int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows) {
+int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
+                      int swizzle_bytes) {
   auto fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -92,10 +93,12 @@ int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, 
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                               : swizzle_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled (u8) failed (CUresult %d)", static_cast<int>(r));
     return SINKATTN_CUDA_ERROR;

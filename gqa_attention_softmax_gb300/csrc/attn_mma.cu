@@ -15,11 +15,15 @@
 //    sum per row, max reduced over the 4-lane quads with warp shuffles),
 //    O += P V with P re-packed to bf16 straight from the S accumulators.
 //  * FP8 KV (e4m3 codes, per-KV-head scales): the producer's TMA copies the
-//    raw codes into the stage ring; the warps of the token group that owns a
-//    tile widen it to f16 (exact: f16 holds every e4m3 value) into their own
-//    128-byte-swizzled tile buffer and run the f16 form of the same MMAs on
-//    it, with Q converted to f16 once. The key scale joins the logit scale,
-//    the value scale multiplies the chunk's accumulator.
+//    raw codes into the stage ring (K codes swizzled in 16-byte chunks). The
+//    S product reads its K fragments straight from the codes -- one 32-bit
+//    load of four adjacent codes per fragment, widened to f16 (exact: f16
+//    holds every e4m3 value) -- with the head dimensions of Q's fragments
+//    relabelled to match, which leaves q . k unchanged. V codes are widened
+//    by the warps of the token group that owns the tile into their own
+//    128-byte-swizzled f16 buffer for the P.V product. Q is converted to f16
+//    once. The key scale joins the logit scale, the value scale multiplies
+//    the chunk's accumulator.
 //  * Tiles are right-aligned to the end of the CTA's key range, so no copy
 //    ever reads past the last key the CTA needs; keys before the range that a
 //    tile covers are masked (and are real data or TMA zero-fill, never NaN).
@@ -284,13 +288,19 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
   }
 
   // Q fragments (A operand, row-major 16 x 16 per k-step), loaded once.
+  // FP8: the k-slots (2c, 2c + 1, 2c + 8, 2c + 9) of lane c = lane % 4 hold
+  // head dims 4c .. 4c + 3 of each 16-dim step, the relabelling under which
+  // the K fragment is one 32-bit load of four adjacent codes; q . k is a sum
+  // over the head dims, so the same relabelling on both operands leaves it
+  // unchanged.
   uint32_t qa[D / 16][4];
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
     for (int reg = 0; reg < 4; ++reg) {
       const int i = reg & 1;
-      const int col = kk * 16 + (lane & 3) * 2 + ((reg >> 1) << 3);
+      const int col = FP8 ? kk * 16 + (lane & 3) * 4 + ((reg >> 1) << 1)
+                          : kk * 16 + (lane & 3) * 2 + ((reg >> 1) << 3);
       uint32_t qv = valid[i]
                         ? *reinterpret_cast<const uint32_t*>(
                               p.q + (static_cast<size_t>(tok[i]) * p.Hq + head[i]) * D + col)
@@ -321,8 +331,9 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
     const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
     uint32_t kbase;
     if constexpr (FP8) {
-      // Widen this tile's e4m3 codes into the group's f16 buffer: each of the
-      // group's RT warps converts every RT-th 16-byte chunk (16 codes).
+      // Widen this tile's V codes into the group's f16 buffer (K is read
+      // straight from the codes by the S product below): each of the group's
+      // RT warps converts every RT-th 16-byte chunk (16 codes).
       const int nt = i / TG;   // the group's tile ordinal
       uint8_t* fb = tiles + tg * C::STAGE_BYTES;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma))) break;
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
       constexpr int CH_ROW = D / 16;        // 16-byte chunks per row of codes
       constexpr int CH_TILE = KT * CH_ROW;
 #pragma unroll 4
-      for (int c = rt * 32 + lane; c < 2 * CH_TILE; c += RT * 32) {
+      for (int c = CH_TILE + rt * 32 + lane; c < 2 * CH_TILE; c += RT * 32) {
         const int tensor = c / CH_TILE;   // 0: K, 1: V
         const int rem = c - tensor * CH_TILE;
         const int row = rem / CH_ROW, cb = rem - row * CH_ROW;
@@ -359,7 +370,6 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch + 1)) = h1;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);   // this warp's codes are read
       if constexpr (RT > 1) {
         if (lane == 0) mbar_arrive(&cvt_done[tg]);
         if (!__all_sync(0xffffffffu, mbar_wait(&cvt_done[tg], nt & 1, abort_flag,
@@ -379,6 +389,28 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
     for (int j = 0; j < KT / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 
     // S = Q K^T
+    if constexpr (FP8) {
+      // K fragments straight from the e4m3 codes: one 32-bit load of four
+      // codes (head dims 4c .. 4c + 3 of the step, lane c = lane % 4) per key
+      // column and 16-dim step, widened to the two f16 pairs of the B
+      // fragment in the relabelled order the Q fragments use
+      // The code rows are swizzled: 16-byte chunk k of key row r sits at chunk
+      // k ^ ((r / 2) % 4) (64-byte rows) or k ^ (r % 8) (128-byte rows); for
+      // r = 8 j + lane / 4 that is a constant of the lane.
+      const int xr = D == 64 ? ((lane >> 3) & 3) : ((lane >> 2) & 7);
+      const uint8_t* kc = f8 + st * C::F8_STAGE + (lane >> 2) * D + (lane & 3) * 4;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int j = 0; j < KT / 8; ++j) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + 8 * j * D + ((kk ^ xr) << 4));
+          mma_f16_16816(s[j], qa[kk], e4m3x2_to_f16x2(static_cast<uint16_t>(w)),
+                        e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);   // this warp has read the tile's codes
+    } else
 #pragma unroll
     for (int kk = 0; kk < D / 16; kk += 2) {
 #pragma unroll
@@ -656,7 +688,10 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
   const uint64_t rows = kv_map_rows(a);
   const int box = kv_box_rows(a, KT);
-  int rc = FP8 ? make_rows_tmap_u8(&tmK, a.k, rows, D, box) : make_rows_tmap(&tmK, a.k, rows, D, box, 128);
+  // FP8: K codes land swizzled (16-byte chunks over the D-byte row), so the
+  // S product's 32-bit fragment loads are free of bank conflicts; V codes,
+  // read linearly by the converters, land plain.
+  int rc = FP8 ? make_rows_tmap_u8(&tmK, a.k, rows, D, box, D) : make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
   rc = FP8 ? make_rows_tmap_u8(&tmV, a.v, rows, D, box) : make_rows_tmap(&tmV, a.v, rows, D, box, 128);
   if (rc) return rc;

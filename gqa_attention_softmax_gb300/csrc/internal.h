@@ -62,8 +62,10 @@ inline int kv_box_rows(const AttnArgs& a, int tile_keys) {
 int make_rows_tmap(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
                    int swizzle_bytes);
 // The same over a [rows, d] array of bytes (e4m3 codes), [box_rows, d] boxes,
-// no swizzle.
-int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows);
+// swizzled in 16-byte chunks over swizzle_bytes (64 or 128; 0: none; the
+// row must be that wide).
+int make_rows_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_rows,
+                      int swizzle_bytes = 0);
 
 // Encodes a 3-D tensor map over q [total_q, Hq, d] bf16 whose box is
 // [QB tokens][G heads][64 columns] (128 rows of one GQA group), 128-byte swizzled.
