@@ -105,6 +105,74 @@ struct TcCfg {
   static_assert(KVSUB % 1024 == 0 && KT % 32 == 0, "tile shape");
 };
 
+// Epilogue: out row = O_t row / l, as bf16. Each lane owns one row of the
+// tile; D / 64 blocks of 64 columns (128 bytes) are read from TMEM, scaled
+// and packed into eight 16-byte chunks. Within each group of 8 lanes an 8 x 8
+// transpose of the chunks (three shfl_xor stages, chunk pairs swapped
+// across lane bit m) leaves lane i with chunk i of each of the group's rows,
+// so a store instruction writes 4 whole 128-byte rows per warp rather than
+// 16 bytes of each of 32 rows: 4 L1 wavefronts instead of 32, which keeps
+// the load/store unit free for the next item's copies into shared memory.
+// Warp-collective; `zero` (warp-uniform) stores zeros without reading TMEM.
+template <int D>
+__device__ __forceinline__ void store_o_rows(uint32_t o_addr, bool zero, float inv,
+                                             __nv_bfloat16* orow, bool valid, int lane) {
+  const int i = lane & 7;
+#pragma unroll
+  for (int blk = 0; blk < D / 64; ++blk) {
+    uint4 ch[8];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float o[32];
+      if (!zero) {
+        tc::tmem_ld32(o_addr + blk * 64 + half * 32, o);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4& pk = ch[half * 4 + q4];
+        pk.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+        pk.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+        pk.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+        pk.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+      }
+    }
+    // stage m: for each chunk pair (e, e | m), the lane with bit m clear
+    // gives chunk e | m and takes its partner's chunk e into that slot; the
+    // partner does the mirror image. After the three stages ch[e] of lane i
+    // is chunk i of the group's row e.
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+      const bool up = (i & m) != 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e & m) continue;
+        const uint4 snd = up ? ch[e] : ch[e | m];
+        uint4 rcv;
+        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
+        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
+        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
+        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
+        if (up) ch[e] = rcv;
+        else ch[e | m] = rcv;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int src = (lane & ~7) + e;
+      const unsigned long long row =
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), src);
+      const int v = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+      if (v)
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(row) + blk * 64 + i * 8) =
+            ch[e];
+    }
+  }
+}
+
 // One block per item: block (x, y, z) runs query block nqb - 1 - x of KV head
 // y of sequence z (longest query blocks launch first), the hardware deals the
 // blocks out to the SMs as they free up.
@@ -503,28 +571,7 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      float o[32];
-      if (n >= 1 && ok) {
-        tc::tmem_ld32(o_addr + c * 32, o);
-        tc::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
-      }
-      if (valid) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 pk;
-          pk.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-          pk.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-          pk.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-          pk.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-          *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = pk;
-        }
-      }
-    }
+    store_o_rows<D>(o_addr, !(n >= 1 && ok), inv, orow, valid, lane);
     if (valid && p.lse != nullptr)
       p.lse[static_cast<size_t>(tok) * p.Hq + h] =
           l > 0.f ? (m_used * c2 + lg2(l)) * kLn2 : kNegInf;
@@ -1079,28 +1126,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        if (n >= 1) {
-          tc::tmem_ld32(o_addr + c * 32, o);
-          tc::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
-        }
-        if (valid) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 pk;
-            pk.x = pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-            pk.y = pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-            pk.z = pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-            pk.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + q4 * 8) = pk;
-          }
-        }
-      }
+      store_o_rows<D>(o_addr, n < 1, inv, orow, valid, lane);
       if (valid && p.lse != nullptr)
         p.lse[static_cast<size_t>(tok) * p.Hq + h] =
             l > 0.f ? (m_used * c2 + lg2(l)) * kLn2 : kNegInf;
@@ -1210,6 +1236,19 @@ static bool prefer_persistent(const AttnArgs& a, int kt) {
   return keys <= 6LL * kt;
 }
 
+// At d 128 both launches run two tiles per CTA, and the persistent one also
+// wins when every SM gets many items, so that the snake order evens out their
+// lengths: Qwen-shaped prefill (3000 items of 2 x 6000 tokens) 1390 against
+// 1340 TFLOP/s. With few long items per SM (1024 items of a 16-draft decode)
+// the hardware's dynamic block dealing balances better (0.69 against
+// 0.73 ms).
+static bool many_items_per_sm(const AttnArgs& a) {
+  const int G = a.Hq / a.Hkv;
+  const long long tokens = 2 * (128 / G);
+  const long long items = (a.max_q + tokens - 1) / tokens * a.Hkv * a.batch;
+  return items >= 16LL * sm_count();
+}
+
 int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   if (G > 128) {
@@ -1222,7 +1261,8 @@ int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
     return launch_tc<64, 4, 3>(a, pers, stream);
   }
   const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
-                    (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<128, 2>::KT));
+                    (kind == SINKATTN_PREFILL_AUTO &&
+                     (prefer_persistent(a, TcCfg<128, 2>::KT) || many_items_per_sm(a)));
   return launch_tc<128, 2, 2>(a, pers, stream);
 }
 
