@@ -15,15 +15,17 @@
 //    sum per row, max reduced over the 4-lane quads with warp shuffles),
 //    O += P V with P re-packed to bf16 straight from the S accumulators.
 //  * FP8 KV (e4m3 codes, per-KV-head scales): the producer's TMA copies the
-//    raw codes into the stage ring (K codes swizzled in 16-byte chunks). The
-//    S product reads its K fragments straight from the codes -- one 32-bit
-//    load of four adjacent codes per fragment, widened to f16 (exact: f16
-//    holds every e4m3 value) -- with the head dimensions of Q's fragments
-//    relabelled to match, which leaves q . k unchanged. V codes are widened
-//    by the warps of the token group that owns the tile into their own
-//    128-byte-swizzled f16 buffer for the P.V product. Q is converted to f16
-//    once. The key scale joins the logit scale, the value scale multiplies
-//    the chunk's accumulator.
+//    raw codes into the stage ring (K and V codes swizzled in 16-byte
+//    chunks), and both products read their fragments straight from the
+//    codes, widened to f16 in registers (exact: f16 holds every e4m3 value).
+//    S: one 32-bit load of four adjacent K codes per fragment, with the head
+//    dimensions of Q's fragments relabelled to match (q . k is unchanged).
+//    P.V: ldmatrix's transposed 8-bit load hands each lane four consecutive
+//    keys of a V column, which become the B fragment's k-slots (2c, 2c + 1,
+//    2c + 8, 2c + 9); S is computed with its key columns permuted to the
+//    same order, so P's fragments need no change (a sum over keys does not
+//    depend on their order). Q is converted to f16 once. The key scale joins
+//    the logit scale, the value scale multiplies the chunk's accumulator.
 //  * Tiles are right-aligned to the end of the CTA's key range, so no copy
 //    ever reads past the last key the CTA needs; keys before the range that a
 //    tile covers are masked (and are real data or TMA zero-fill, never NaN).
@@ -84,17 +86,17 @@ struct MmaCfg {
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int F8_TILE = KT * D;           // one K or V tile of e4m3 codes
   static constexpr int F8_STAGE = 2 * F8_TILE;
-  // bf16: the stage ring of tiles; FP8: one f16 tile buffer per token group,
-  // then the ring of e4m3 stages
-  static constexpr int OFF_F8 = FP8 ? TG * STAGE_BYTES : NST * STAGE_BYTES;
+  // bf16: the stage ring of tiles; FP8: the ring of e4m3 stages
+  static constexpr int OFF_F8 = FP8 ? 0 : NST * STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_F8 + (FP8 ? NST * F8_STAGE : 0);
   static constexpr int XCHG_FLOATS_PER_LANE = D / 2 + 4;
   static constexpr int XCHG_BYTES = (TG - 1) * RT * 32 * XCHG_FLOATS_PER_LANE * 4;
-  static constexpr int BAR_BYTES = (2 * NST + 2 * TG) * 8 + 16;
+  static constexpr int BAR_BYTES = 2 * NST * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES + XCHG_BYTES;
   // fused mode: one CTA's partial, [16 RT rows][m, d, pad, pad, acc[D]], over the tile ring
   static constexpr int XOUT_STRIDE = D + 4;
-  static_assert(16 * RT * XOUT_STRIDE * 4 <= NST * STAGE_BYTES, "partial fits in the tile ring");
+  static_assert(FP8 || 16 * RT * XOUT_STRIDE * 4 <= NST * STAGE_BYTES,
+                "partial fits in the tile ring");
   // Two resident CTAs per SM: one CTA's prologue (barrier set-up, first TMA
   // round trip, Q fragments) and epilogue overlap the other's streaming.
   static constexpr int MIN_CTAS = 2;
@@ -112,14 +114,12 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* tiles = smem;                 // bf16: stage ring; FP8: f16 buffer per token group
+  uint8_t* tiles = smem;                 // bf16: stage ring
   uint8_t* f8 = smem + C::OFF_F8;        // FP8: e4m3 stage ring [NST][K | V]
   // bf16: full / empty of the stage ring; FP8: codes landed / codes read
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + NST;
-  uint64_t* cvt_done = empty + NST;      // FP8, RT > 1: [TG] the group's tile is converted
-  uint64_t* buf_free = cvt_done + TG;    // FP8, RT > 1: [TG] the group's buffer was read
-  int* abort_flag = reinterpret_cast<int*>(buf_free + TG);
+  int* abort_flag = reinterpret_cast<int*>(empty + NST);
   float* xchg = reinterpret_cast<float*>(smem + C::OFF_BAR + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5;
@@ -162,10 +162,6 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], RT);
     }
-    for (int i = 0; i < TG; ++i) {
-      mbar_init(&cvt_done[i], RT);
-      mbar_init(&buf_free[i], RT);
-    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -200,7 +196,7 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
         const int j0 = first + i * KT;
         if constexpr (FP8) {
-          // e4m3 codes into the code ring; the converter warps fill `full`
+          // e4m3 codes into the code ring
           if (!__all_sync(members, mbar_wait(&empty[st], ph ^ 1u, abort_flag, &g_status_attn_mma)))
             break;
           if (i == skip_tile) {   // test hook: the waits for this tile run out
@@ -329,54 +325,9 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
   for (int i = tg; i < ntiles; i += TG) {
     const int st = i % NST;
     const uint32_t ph = static_cast<uint32_t>(i / NST) & 1u;
-    uint32_t kbase;
+    uint32_t kbase = 0;
     if constexpr (FP8) {
-      // Widen this tile's V codes into the group's f16 buffer (K is read
-      // straight from the codes by the S product below): each of the group's
-      // RT warps converts every RT-th 16-byte chunk (16 codes).
-      const int nt = i / TG;   // the group's tile ordinal
-      uint8_t* fb = tiles + tg * C::STAGE_BYTES;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma))) break;
-      if constexpr (RT > 1) {   // every warp of the group has read the previous tile
-        if (nt > 0 && !__all_sync(0xffffffffu, mbar_wait(&buf_free[tg], (nt - 1) & 1, abort_flag,
-                                                         &g_status_attn_mma)))
-          break;
-      } else {
-        __syncwarp();
-      }
-      const uint8_t* codes = f8 + st * C::F8_STAGE;
-      constexpr int CH_ROW = D / 16;        // 16-byte chunks per row of codes
-      constexpr int CH_TILE = KT * CH_ROW;
-#pragma unroll 4
-      for (int c = CH_TILE + rt * 32 + lane; c < 2 * CH_TILE; c += RT * 32) {
-        const int tensor = c / CH_TILE;   // 0: K, 1: V
-        const int rem = c - tensor * CH_TILE;
-        const int row = rem / CH_ROW, cb = rem - row * CH_ROW;
-        const uint4 w =
-            *reinterpret_cast<const uint4*>(codes + tensor * C::F8_TILE + row * D + cb * 16);
-        uint4 h0, h1;
-        h0.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x));
-        h0.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16));
-        h0.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y));
-        h0.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16));
-        h1.x = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z));
-        h1.y = e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16));
-        h1.z = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w));
-        h1.w = e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16));
-        // columns 16 cb .. 16 cb + 15: sub-tile cb / 4, 16-byte chunks 2 (cb % 4) and + 1
-        uint8_t* sub = fb + tensor * C::TILE_BYTES + (cb >> 2) * C::SUB_BYTES;
-        const int ch = (cb & 3) * 2;
-        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch)) = h0;
-        *reinterpret_cast<uint4*>(sub + sw128_offset(row, ch + 1)) = h1;
-      }
-      __syncwarp();
-      if constexpr (RT > 1) {
-        if (lane == 0) mbar_arrive(&cvt_done[tg]);
-        if (!__all_sync(0xffffffffu, mbar_wait(&cvt_done[tg], nt & 1, abort_flag,
-                                               &g_status_attn_mma)))
-          break;
-      }
-      kbase = smem_u32(fb);
     } else {
       if (!mbar_wait(&full[st], ph, abort_flag, &g_status_attn_mma)) break;
       kbase = smem_u32(tiles + st * C::STAGE_BYTES);
@@ -393,23 +344,32 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
       // K fragments straight from the e4m3 codes: one 32-bit load of four
       // codes (head dims 4c .. 4c + 3 of the step, lane c = lane % 4) per key
       // column and 16-dim step, widened to the two f16 pairs of the B
-      // fragment in the relabelled order the Q fragments use
+      // fragment in the relabelled order the Q fragments use. Block j of S
+      // holds, in column n, key 16 (j / 2) + kr(n) + 2 (j % 2) with
+      // kr(n) = 2n - (n % 2): the order in which the P.V product below takes
+      // its V fragments.
       // The code rows are swizzled: 16-byte chunk k of key row r sits at chunk
       // k ^ ((r / 2) % 4) (64-byte rows) or k ^ (r % 8) (128-byte rows); for
-      // r = 8 j + lane / 4 that is a constant of the lane.
-      const int xr = D == 64 ? ((lane >> 3) & 3) : ((lane >> 2) & 7);
-      const uint8_t* kc = f8 + st * C::F8_STAGE + (lane >> 2) * D + (lane & 3) * 4;
+      // r = 16 i + kr(lane / 4) + 2 (j % 2) that is a constant of the lane.
+      const int kr = 2 * (lane >> 2) - ((lane >> 2) & 1);
+      int xr[2];
+      const uint8_t* kc[2];
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const int r = kr + 2 * blk;
+        xr[blk] = D == 64 ? ((r >> 1) & 3) : (r & 7);
+        kc[blk] = f8 + st * C::F8_STAGE + r * D + (lane & 3) * 4;
+      }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
         for (int j = 0; j < KT / 8; ++j) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + 8 * j * D + ((kk ^ xr) << 4));
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(kc[j & 1] + 16 * (j >> 1) * D +
+                                                                ((kk ^ xr[j & 1]) << 4));
           mma_f16_16816(s[j], qa[kk], e4m3x2_to_f16x2(static_cast<uint16_t>(w)),
                         e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);   // this warp has read the tile's codes
     } else
 #pragma unroll
     for (int kk = 0; kk < D / 16; kk += 2) {
@@ -437,7 +397,8 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
       for (int j = 0; j < KT / 8; ++j) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = j0 + 8 * j + (lane & 3) * 2 + (e & 1);
+          const int key = FP8 ? j0 + 16 * (j >> 1) + 4 * (lane & 3) + 2 * (j & 1) + (e & 1)
+                              : j0 + 8 * j + (lane & 3) * 2 + (e & 1);
           const int ps = pos[e >> 1];
           const bool vis = key >= k_lo && key < k_hi && (!p.causal || key <= ps) &&
                            (p.window <= 0 || key > ps - p.window);
@@ -497,28 +458,39 @@ __global__ void __launch_bounds__(MmaCfg<D, RT, TG, KT, NST, FP8>::THREADS,
         a[2] = pack_bf16x2(s[2 * kt2 + 1][0], s[2 * kt2 + 1][1]);
         a[3] = pack_bf16x2(s[2 * kt2 + 1][2], s[2 * kt2 + 1][3]);
       }
+      if constexpr (FP8) {
+        // V fragments straight from the codes: the transposed 8-bit load of
+        // keys 16 kt2 .. + 15 x columns 16 jd2 .. + 15 gives lane (g, c) keys
+        // 4c .. 4c + 3 of columns g and g + 8, the k-slots (2c, 2c + 1,
+        // 2c + 8, 2c + 9) of the B fragments in the key order of S above.
+        // Lanes 0-15 address the 16 key rows (swizzled like K's).
+        const int vr = lane & 15;
+        const int vxr = D == 64 ? ((vr >> 1) & 3) : (vr & 7);
+        const uint8_t* vrow = f8 + st * C::F8_STAGE + C::F8_TILE + (16 * kt2 + vr) * D;
 #pragma unroll
-      for (int jd = 0; jd < D / 8; jd += 2) {
-        const int mi = lane >> 3;
-        const int trow = 16 * kt2 + (mi & 1) * 8 + (lane & 7);
-        const int chunk = jd + (mi >> 1);
-        uint32_t bf[4];
-        ldsm_x4_trans(bf, vbase + (chunk >> 3) * C::SUB_BYTES + sw128_offset(trow, chunk & 7));
-        if constexpr (FP8) {
-          mma_f16_16816(o[jd], a, bf[0], bf[1]);
-          mma_f16_16816(o[jd + 1], a, bf[2], bf[3]);
-        } else {
+        for (int jd2 = 0; jd2 < D / 16; ++jd2) {
+          uint32_t r0, r1;
+          ldsm_b8_trans(r0, r1, smem_u32(vrow + ((jd2 ^ vxr) << 4)));
+          mma_f16_16816(o[2 * jd2], a, e4m3x2_to_f16x2(static_cast<uint16_t>(r0)),
+                        e4m3x2_to_f16x2(static_cast<uint16_t>(r0 >> 16)));
+          mma_f16_16816(o[2 * jd2 + 1], a, e4m3x2_to_f16x2(static_cast<uint16_t>(r1)),
+                        e4m3x2_to_f16x2(static_cast<uint16_t>(r1 >> 16)));
+        }
+      } else {
+#pragma unroll
+        for (int jd = 0; jd < D / 8; jd += 2) {
+          const int mi = lane >> 3;
+          const int trow = 16 * kt2 + (mi & 1) * 8 + (lane & 7);
+          const int chunk = jd + (mi >> 1);
+          uint32_t bf[4];
+          ldsm_x4_trans(bf, vbase + (chunk >> 3) * C::SUB_BYTES + sw128_offset(trow, chunk & 7));
           mma_bf16_16816(o[jd], a, bf[0], bf[1]);
           mma_bf16_16816(o[jd + 1], a, bf[2], bf[3]);
         }
       }
     }
     __syncwarp();
-    if constexpr (FP8) {
-      if (RT > 1 && lane == 0) mbar_arrive(&buf_free[tg]);   // the group's buffer is read
-    } else {
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
+    if (lane == 0) mbar_arrive(&empty[st]);   // this warp has read the tile
   }
 
   // Row sums are split over the 4 lanes of each quad.
@@ -688,12 +660,12 @@ static int launch_cfg(const AttnArgs& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
   const uint64_t rows = kv_map_rows(a);
   const int box = kv_box_rows(a, KT);
-  // FP8: K codes land swizzled (16-byte chunks over the D-byte row), so the
-  // S product's 32-bit fragment loads are free of bank conflicts; V codes,
-  // read linearly by the converters, land plain.
+  // FP8: K and V codes land swizzled (16-byte chunks over the D-byte row), so
+  // the S product's 32-bit fragment loads and the P.V product's transposed
+  // 16-row loads are free of bank conflicts.
   int rc = FP8 ? make_rows_tmap_u8(&tmK, a.k, rows, D, box, D) : make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
-  rc = FP8 ? make_rows_tmap_u8(&tmV, a.v, rows, D, box) : make_rows_tmap(&tmV, a.v, rows, D, box, 128);
+  rc = FP8 ? make_rows_tmap_u8(&tmV, a.v, rows, D, box, D) : make_rows_tmap(&tmV, a.v, rows, D, box, 128);
   if (rc) return rc;
 
   MmaParams p{};
@@ -776,16 +748,19 @@ static int launch_attn_mma_t(const AttnArgs& a, cudaStream_t stream) {
     set_error("GQA group of %d query heads exceeds 64 rows per CTA", G);
     return SINKATTN_UNSUPPORTED;
   }
+  // stages of the ring: an FP8 stage holds half the bytes of a bf16 one, so
+  // twice as many keep the same bytes in flight per SM
+  constexpr int NS = FP8 ? 8 : 4;
   if (a.d == 64) {
-    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, 4, FUSED, FP8>(a, stream);
-    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, 4, FUSED, FP8>(a, stream);
-    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, 4, FUSED, FP8>(a, stream);
-    return launch_cfg<64, 4, 2, 64, 4, FUSED, FP8>(a, stream);
+    if (rt_needed <= 1) return launch_cfg<64, 1, 4, 64, NS, FUSED, FP8>(a, stream);
+    if (rt_needed <= 2) return launch_cfg<64, 2, 2, 64, NS, FUSED, FP8>(a, stream);
+    if (rt_needed <= 3) return launch_cfg<64, 3, 2, 64, NS, FUSED, FP8>(a, stream);
+    return launch_cfg<64, 4, 2, 64, NS, FUSED, FP8>(a, stream);
   }
-  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, 4, FUSED, FP8>(a, stream);
-  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, 4, FUSED, FP8>(a, stream);
-  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, 4, FUSED, FP8>(a, stream);
-  return launch_cfg<128, 4, 2, 32, 4, FUSED, FP8>(a, stream);
+  if (rt_needed <= 1) return launch_cfg<128, 1, 4, 32, NS, FUSED, FP8>(a, stream);
+  if (rt_needed <= 2) return launch_cfg<128, 2, 2, 32, NS, FUSED, FP8>(a, stream);
+  if (rt_needed <= 3) return launch_cfg<128, 3, 2, 32, NS, FUSED, FP8>(a, stream);
+  return launch_cfg<128, 4, 2, 32, NS, FUSED, FP8>(a, stream);
 }
 
 int launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {

@@ -166,6 +166,15 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr));
 }
 
+// A 16 x 16 matrix of bytes, transposed: lanes 0-15 address rows 0-15 (16
+// bytes each); lane (g, c) = (lane / 4, lane % 4) receives rows 4c .. 4c + 3
+// of column g in r0 and of column g + 8 in r1, row 4c in the lowest byte.
+__device__ __forceinline__ void ldsm_b8_trans(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
