@@ -329,6 +329,34 @@ __device__ __forceinline__ void ld_dsmem_vec(const float* p, uint32_t rank, floa
   }
 }
 
+// Within each group of 8 lanes, lane i holds chunk e (e = 0..7, 16 bytes
+// each) of row i of the group in ch[e]; afterwards it holds chunk i of row e
+// in ch[e]. Three shfl_xor stages: at lane bit m, for each chunk pair
+// (e, e | m), the lane with bit m clear gives chunk e | m and takes its
+// partner's chunk e into that slot, and the partner does the mirror image.
+// Rows stored as ch[e] of lane i at chunk i then make a store instruction
+// write 4 whole 128-byte row segments per warp. Warp-collective.
+template <typename V4>
+__device__ __forceinline__ void transpose8_chunks(V4 (&ch)[8], int lane) {
+  const int i = lane & 7;
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool up = (i & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e & m) continue;
+      V4 snd = up ? ch[e] : ch[e | m];
+      V4 rcv;
+      rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
+      rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
+      rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
+      rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
+      if (up) ch[e] = rcv;
+      else ch[e | m] = rcv;
+    }
+  }
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

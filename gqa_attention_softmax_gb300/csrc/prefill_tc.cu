@@ -107,12 +107,12 @@ struct TcCfg {
 
 // Epilogue: out row = O_t row / l, as bf16. Each lane owns one row of the
 // tile; D / 64 blocks of 64 columns (128 bytes) are read from TMEM, scaled
-// and packed into eight 16-byte chunks. Within each group of 8 lanes an 8 x 8
-// transpose of the chunks (three shfl_xor stages, chunk pairs swapped
-// across lane bit m) leaves lane i with chunk i of each of the group's rows,
-// so a store instruction writes 4 whole 128-byte rows per warp rather than
-// 16 bytes of each of 32 rows: 4 L1 wavefronts instead of 32, which keeps
-// the load/store unit free for the next item's copies into shared memory.
+// and packed into eight 16-byte chunks. An 8 x 8 transpose of the chunks
+// within each group of 8 lanes leaves lane i with chunk i of each of the
+// group's rows, so a store instruction writes 4 whole 128-byte rows per warp
+// rather than 16 bytes of each of 32 rows: 4 L1 wavefronts instead of 32,
+// which keeps the load/store unit free for the next item's copies into
+// shared memory.
 // Warp-collective; `zero` (warp-uniform) stores zeros without reading TMEM.
 template <int D>
 __device__ __forceinline__ void store_o_rows(uint32_t o_addr, bool zero, float inv,
@@ -140,26 +140,7 @@ __device__ __forceinline__ void store_o_rows(uint32_t o_addr, bool zero, float i
         pk.w = pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
       }
     }
-    // stage m: for each chunk pair (e, e | m), the lane with bit m clear
-    // gives chunk e | m and takes its partner's chunk e into that slot; the
-    // partner does the mirror image. After the three stages ch[e] of lane i
-    // is chunk i of the group's row e.
-#pragma unroll
-    for (int m = 4; m >= 1; m >>= 1) {
-      const bool up = (i & m) != 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (e & m) continue;
-        const uint4 snd = up ? ch[e] : ch[e | m];
-        uint4 rcv;
-        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
-        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
-        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
-        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
-        if (up) ch[e] = rcv;
-        else ch[e | m] = rcv;
-      }
-    }
+    transpose8_chunks(ch, lane);   // now ch[e] of lane i: chunk i of the group's row e
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int src = (lane & ~7) + e;
