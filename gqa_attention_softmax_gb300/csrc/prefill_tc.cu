@@ -9,8 +9,8 @@
 //    head -- each tile is QB = 128/G consecutive tokens times the G query
 //    heads sharing that KV head -- so one K/V tile in shared memory serves
 //    every tile and the whole GQA group, and the causal diagonal cuts only a
-//    few keys of the last KV tile. NT is 3 at head_dim 64 in the one-block
-//    launch, 2 otherwise;
+//    few keys of the last KV tile. NT is 3 at head_dim 64 and 2 at 128, in
+//    both launches;
 //  * warp 0: TMA producer (the Q tiles once as 3-D boxes, then K/V tiles of
 //    KT keys -- 96 at head_dim 64, 128 at 128 -- into an NST-stage ring,
 //    right-aligned to the end of the key range so no copy reads past the
@@ -21,9 +21,7 @@
 //    P_t read from TMEM, V from shared memory). With one S buffer per tile
 //    the order is S_t(0) for every tile, then per KV tile j and tile t:
 //    PV_t(j), then S_t(j+1) once PV_t(j) has completed (S overwrites P), so
-//    the tiles' chains interleave on the tensor core. The two-tile
-//    persistent launch at head_dim 64 shares four S buffers round-robin and
-//    keeps S three steps ahead of P.V;
+//    the tiles' chains interleave on the tensor core;
 //  * warps 2 + 4t .. 5 + 4t: softmax of tile t, one thread per row (= TMEM
 //    lane). The running max starts at the head's sink and the running sum at
 //    1 ("GPT-OSS on Day 0", section "Kernels for GPT-OSS / Sink attention").
@@ -63,16 +61,12 @@ struct TcParams {
 
 template <int D, int NST, int NT = 2>
 struct TcCfg {
-  // NT query tiles per CTA (one softmax warpgroup each). Two tiles at d 64:
-  // four S buffers shared round-robin, so S is issued three steps ahead of
-  // the P.V that frees its buffer and the tensor core always has queued
-  // work. Otherwise one S buffer per tile (three tiles at d 64, two at d 128:
-  // TMEM holds no more).
-  static constexpr bool RING = (D == 64 && NT == 2);
+  // NT query tiles per CTA (one softmax warpgroup each), one S buffer per
+  // tile: three tiles at d 64, two at d 128 (TMEM holds no more).
   static constexpr int NO = D;                    // O_t columns
   static constexpr int NSUB = D / 64;
   static constexpr int KT = D == 64 ? 96 : 128;   // keys per KV tile
-  static constexpr int NSB = RING ? 4 : NT;       // S buffers
+  static constexpr int NSB = NT;                  // S buffers
   static constexpr int QSUB = 128 * 128;          // [128 rows][64 bf16], 128B-swizzled: 16 KB
   static constexpr int KVSUB = KT * 128;          // [KT rows][64 bf16], 128B-swizzled
   static constexpr int Q_TILE = NSUB * QSUB;
@@ -84,7 +78,7 @@ struct TcCfg {
   static constexpr int CUQ_CAP = 1025;            // sequences staged for the item scan
   static constexpr int OFF_LIST = OFF_KV + NST * STAGE;   // [LIST_CAP + 32 + CUQ_CAP] ints
   static constexpr int OFF_BAR = OFF_LIST + ((LIST_CAP + 32 + CUQ_CAP) * 4 + 15) / 16 * 16;
-  static constexpr int N_BARS = 2 + 2 * NST + NSB + NT + NT + NSB + 1;
+  static constexpr int N_BARS = 2 + 2 * NST + NSB + NT + NT + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + N_BARS * 8 + 64;
   static constexpr int THREADS = (2 + 4 * NT) * 32;   // TMA, MMA, NT tiles x 4 softmax warps
   // registers per thread: 14 warps put 4 on two SM sub-partitions, whose
@@ -97,9 +91,6 @@ struct TcCfg {
   __host__ __device__ static constexpr uint32_t col_o(int t) {
     return static_cast<uint32_t>(NSB * KT + NO * t);
   }
-  // S buffer of tile t at KV tile j, and how many times it was filled before
-  __host__ __device__ static constexpr int buf_of(int t, int j) { return RING ? (2 * j + t) % NSB : t; }
-  __host__ __device__ static constexpr int use_of(int t, int j) { return RING ? (2 * j + t) / NSB : j; }
   static_assert(NSB * KT + NT * NO <= 512, "TMEM budget");
   static_assert(NT == 2 || (NT == 3 && D == 64), "tiles per CTA");
   static_assert(KVSUB % 1024 == 0 && KT % 32 == 0, "tile shape");
@@ -322,7 +313,7 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
       const uint32_t v_base0 = smem_u32(smem + C::OFF_KV + C::KV_TILE);
       const uint64_t vd0 = tc::smem_desc_sw128(v_base0, static_cast<uint32_t>(C::KVSUB), 1024);
       auto issue_s = [&](int t, int j) {
-        const int buf = C::buf_of(t, j);
+        const int buf = t;
         const uint64_t kd = kd0 + static_cast<uint64_t>(j % NST) * STAGE16;
         const uint64_t qd = qd0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
         const uint32_t d_tm = tmem + C::col_s(buf);
@@ -341,7 +332,7 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
       auto issue_pv = [&](int t, int j) {
         const uint64_t vd = vd0 + static_cast<uint64_t>(j % NST) * STAGE16;
         const uint32_t d_tm = tmem + C::col_o(t);
-        const uint32_t a_tm = tmem + C::col_s(C::buf_of(t, j));
+        const uint32_t a_tm = tmem + C::col_s(t);
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
@@ -354,22 +345,12 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
       // Order, one buffer per tile: S_t(0) for every tile, then per KV tile j
       // and tile t: PV_t(j), then S_t(j+1) into the same buffer once PV_t(j) is
       // done (the tensor core may not overwrite P before the MMA has read it).
-      // Ring of four, with k = 2 j + t the step's rank: S(0) S(1) S(2), then
-      // per step PV(k), then S(k + 3) into the buffer of PV(k - 1) once that
-      // is done -- PV(k) is queued meanwhile, so the tensor core never drains.
       bool ok = wwait1(q_full, 0);
       if (ok && n > 0) {
         ok = wwait1(&kv_full[0], 0);
         if (ok) {
           tc::fence_after_sync();
           for (int t = 0; t < NT; ++t) issue_s(t, 0);
-        }
-        if (ok && C::RING && n > 1) {
-          ok = wwait1(&kv_full[1 % NST], (1 / NST) & 1);
-          if (ok) {
-            tc::fence_after_sync();
-            issue_s(0, 1);
-          }
         }
       }
       for (int j = 0; ok && j < n; ++j) {
@@ -381,23 +362,13 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
             if (leader) tc::commit(&kv_empty[j % NST]);
             __syncwarp();
           }
-          const int tn = C::RING ? 1 - t : t;
-          const int jn = C::RING ? j + 1 + t : j + 1;
-          if (jn < n) {
-            // a tile's first S of KV tile jn waits for its K
-            if (tn == 0 && !wwait1(&kv_full[jn % NST], (jn / NST) & 1)) { ok = false; break; }
-            // the PV whose buffer the next S overwrites: PV_t(j) with one
-            // buffer per tile; with the ring, the step before (PV_B(j-1) or
-            // PV_A(j))
-            if (!C::RING) {
-              if (!wwait1(&pv_done[t], j & 1)) { ok = false; break; }
-            } else if (t == 1) {
-              if (!wwait1(&pv_done[0], j & 1)) { ok = false; break; }
-            } else if (j >= 1) {
-              if (!wwait1(&pv_done[1], (j - 1) & 1)) { ok = false; break; }
-            }
+          if (j + 1 < n) {
+            // the first tile's S of KV tile j + 1 waits for its K; S_t(j + 1)
+            // overwrites the buffer PV_t(j) reads P from
+            if (t == 0 && !wwait1(&kv_full[(j + 1) % NST], ((j + 1) / NST) & 1)) { ok = false; break; }
+            if (!wwait1(&pv_done[t], j & 1)) { ok = false; break; }
             tc::fence_after_sync();
-            issue_s(tn, jn);
+            issue_s(t, j + 1);
           }
         }
       }
@@ -446,8 +417,8 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
     };
 
     for (int j = 0; j < n; ++j) {
-      const int buf = C::buf_of(t, j);
-      if (!wwait(&s_full[buf], C::use_of(t, j) & 1)) { ok = false; break; }
+      const int buf = t;
+      if (!wwait(&s_full[buf], j & 1)) { ok = false; break; }
       tc::fence_after_sync();
       const uint32_t s_addr = lane_base + C::col_s(buf);
       const int j0 = first + j * KT;
@@ -519,13 +490,8 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
       const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
       const float rs = rsa.x + rsa.y;
 
-      // Ring: PV_t(j-1) has completed before O_t is touched or P_t(j) is
-      // handed over (so p_full[t] cannot run two phases ahead of the MMA
-      // warp). With one buffer per tile S_t(j) was issued after PV_t(j-1).
-      if (C::RING && j >= 1) {
-        if (!wwait(&pv_done[t], (j - 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-      }
+      // S_t(j) was issued after PV_t(j-1) had completed, so O_t is free to
+      // touch and p_full[t] cannot run two phases ahead of the MMA warp.
       // Rescale the row's O_t when some row of this warp moved its maximum
       // (warp-uniform branch).
       if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
@@ -582,7 +548,7 @@ struct PfItem {
   int b, kvh, q_start, Lq, q0, nq, k_start, Lk, pos0, k_lo, k_hi, n, first;
 };
 
-template <int KT>
+template <int KT, int NT>
 __device__ __forceinline__ PfItem pf_item(const TcParams& p, int it) {
   PfItem t;
   const int per = p.Hkv * p.batch;
@@ -594,12 +560,12 @@ __device__ __forceinline__ PfItem pf_item(const TcParams& p, int it) {
   t.Lq = p.cu_q ? p.cu_q[t.b + 1] - t.q_start : p.q_len;
   t.k_start = p.cu_k[t.b];
   t.Lk = p.cu_k[t.b + 1] - t.k_start;
-  t.q0 = qb * 2 * p.QB;   // first token of tile A
+  t.q0 = qb * NT * p.QB;   // first token of the item's first tile
   t.nq = 0;
   t.pos0 = t.k_lo = t.k_hi = t.first = 0;
   t.n = -1;
   if (t.q0 >= t.Lq) return t;
-  t.nq = min(2 * p.QB, t.Lq - t.q0);
+  t.nq = min(NT * p.QB, t.Lq - t.q0);
   t.pos0 = t.Lk - t.Lq + t.q0;
   const int posN = t.pos0 + t.nq - 1;
   t.k_hi = t.Lk;
@@ -619,12 +585,12 @@ __device__ __forceinline__ PfItem pf_item(const TcParams& p, int it) {
 // across items, so the K/V ring streams on from one item into the next; the
 // next item's Q is loaded as soon as the tensor core has finished the
 // current item's last S.
-template <int D, int NST>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int NST, int NT>
+__global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
     prefill_tc_persistent_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
-  using C = TcCfg<D, NST>;
+  using C = TcCfg<D, NST, NT>;
   constexpr int KT = C::KT;
 
   extern __shared__ uint8_t smem_raw[];
@@ -636,10 +602,9 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = q_empty + 1;
   uint64_t* kv_empty = kv_full + NST;
   uint64_t* s_full = kv_empty + NST;   // [NSB]: S written into buffer b
-  uint64_t* p_full = s_full + C::NSB;  // [2]: P_t written and O_t rescaled (128 arrivals)
-  uint64_t* pv_done = p_full + 2;      // [2]: PV_t completed (one buffer per tile)
-  uint64_t* pv_buf = pv_done + 2;      // [NSB]: the P.V reading buffer b completed (ring)
-  uint64_t* drain = pv_buf + C::NSB;
+  uint64_t* p_full = s_full + C::NSB;  // [NT]: P_t written and O_t rescaled (128 arrivals)
+  uint64_t* pv_done = p_full + NT;     // [NT]: PV_t completed (one buffer per tile)
+  uint64_t* drain = pv_done + NT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* status = &g_status_prefill_tc;
@@ -657,11 +622,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < C::NSB; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&pv_buf[i], 1);
-    }
-    for (int t = 0; t < 2; ++t) {
+    for (int i = 0; i < C::NSB; ++i) mbar_init(&s_full[i], 1);
+    for (int t = 0; t < NT; ++t) {
       mbar_init(&p_full[t], 128);
       mbar_init(&pv_done[t], 1);
     }
@@ -690,7 +652,7 @@ __global__ void __launch_bounds__(320, 1)
     const int qb = p.nqb - 1 - it / per;
     const int b = (it % per) / p.Hkv;
     const int Lq = staged ? cuq_s[b + 1] - cuq_s[b] : (p.cu_q ? p.cu_q[b + 1] - p.cu_q[b] : p.q_len);
-    return qb * 2 * p.QB < Lq;
+    return qb * NT * p.QB < Lq;
   };
   int n_list = 0, total = 0;
   bool use_list = staged;
@@ -753,12 +715,12 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmV);
     }
     const uint64_t policy = policy_evict_last();   // K/V are re-read by every query block
-    const uint32_t q_bytes = static_cast<uint32_t>(2 * C::NSUB * 128 * p.G * p.QB);
+    const uint32_t q_bytes = static_cast<uint32_t>(NT * C::NSUB * 128 * p.G * p.QB);
     int g = 0, qi = 0;   // KV tiles and active items so far
     bool ok = true;
     const int skip_tile = hook_skip_tile();
     for (int k = 0; ok && k < n_mine; ++k) {
-      const PfItem t = pf_item<KT>(p, item_of(k));
+      const PfItem t = pf_item<KT, NT>(p, item_of(k));
       if (t.n < 0) continue;
       if (leader && (t.Lk < t.Lq || t.Lk > p.max_kv)) atomicExch(status, SINKATTN_BAD_LENGTHS);
       if (t.n == 0) continue;
@@ -766,7 +728,7 @@ __global__ void __launch_bounds__(320, 1)
       if (leader) {
         mbar_arrive_expect_tx(q_full, q_bytes);
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt)
+        for (int tt = 0; tt < NT; ++tt)
 #pragma unroll
           for (int sub = 0; sub < C::NSUB; ++sub)
             tc::tma_load_3d(smem + C::OFF_Q + tt * C::Q_TILE + sub * C::QSUB, &tmQ, sub * 64,
@@ -843,7 +805,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t vd0 = tc::smem_desc_sw128(v_base0, static_cast<uint32_t>(C::KVSUB), 1024);
     // S_t of global KV tile g
     auto issue_s = [&](int t, int g) {
-      const int buf = C::buf_of(t, g);
+      const int buf = t;
       const uint64_t kd = kd0 + static_cast<uint64_t>(g % NST) * STAGE16;
       const uint64_t qd = qd0 + static_cast<uint64_t>(t) * (C::Q_TILE >> 4);
       const uint32_t d_tm = tmem + C::col_s(buf);
@@ -863,15 +825,13 @@ __global__ void __launch_bounds__(320, 1)
     auto issue_pv = [&](int t, int g, bool first_of_item) {
       const uint64_t vd = vd0 + static_cast<uint64_t>(g % NST) * STAGE16;
       const uint32_t d_tm = tmem + C::col_o(t);
-      const uint32_t a_tm = tmem + C::col_s(C::buf_of(t, g));
+      const uint32_t a_tm = tmem + C::col_s(t);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
           tc::mma_ts(d_tm, a_tm + kk * 8, vd + static_cast<uint64_t>(kk) * 128u, idesc_o,
                      (!first_of_item || kk > 0) ? 1u : 0u);
-        // ring: one barrier per S buffer (the buffer's next S waits for it);
-        // one buffer per tile: one barrier per tile
-        tc::commit(C::RING ? &pv_buf[C::buf_of(t, g)] : &pv_done[t]);
+        tc::commit(&pv_done[t]);   // S_t of the next KV tile may overwrite P_t
       }
       __syncwarp();
     };
@@ -882,59 +842,32 @@ __global__ void __launch_bounds__(320, 1)
     int g = 0, qi = 0;   // KV tiles and active items so far
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
-      const PfItem t = pf_item<KT>(p, item_of(k));
+      const PfItem t = pf_item<KT, NT>(p, item_of(k));
       if (t.n <= 0) continue;
       if (!wwait1(q_full, qi & 1)) { ok = false; break; }
       const int g0 = g, n = t.n;
-      if constexpr (C::RING) {
-        // Steps ranked k = 2 g + t (tile t at global KV tile g). S(k0 .. k0+2)
-        // of the item, then per step PV(k) and S(k + 3), the latter into the
-        // buffer of PV(k - 1) once that has completed; PV(k) is queued
-        // meanwhile, so the tensor core does not drain at the hand-off.
-        const int k0 = 2 * g0, kend = 2 * (g0 + n);
-        auto s_step = [&](int k) -> bool {
-          const int gt = k >> 1, tt = k & 1;
-          if (tt == 0 && !wwait1(&kv_full[gt % NST], (gt / NST) & 1)) return false;
-          if (k >= C::NSB && !wwait1(&pv_buf[k % C::NSB], ((k - C::NSB) / C::NSB) & 1))
-            return false;
+      // One buffer per tile: S_t(g0) of every tile, then per KV tile g and
+      // tile t: PV_t(g), then S_t(g+1) into the same buffer once PV_t(g) is done.
+      for (int tt = 0; ok && tt < NT; ++tt) {
+        if (tt == 0 && !wwait1(&kv_full[g0 % NST], (g0 / NST) & 1)) { ok = false; break; }
+        if (g0 > 0 && !wwait1(&pv_done[tt], (g0 - 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        issue_s(tt, g0);
+        if (n == 1 && tt == NT - 1) commit1(q_empty);
+      }
+      for (int jj = 0; ok && jj < n; ++jj) {
+        const int gg = g0 + jj;
+        for (int tt = 0; tt < NT; ++tt) {
+          if (!wwait1(&p_full[tt], gg & 1)) { ok = false; break; }
           tc::fence_after_sync();
-          issue_s(tt, gt);
-          if (k == kend - 1) commit1(q_empty);   // the item's last S: Q may be replaced
-          return true;
-        };
-        for (int k = k0; ok && k < min(k0 + 3, kend); ++k) ok = s_step(k);
-        for (int k = k0; ok && k < kend; ++k) {
-          const int gt = k >> 1, tt = k & 1;
-          if (!wwait1(&p_full[tt], gt & 1)) { ok = false; break; }
-          tc::fence_after_sync();
-          issue_pv(tt, gt, gt == g0);
-          if (tt == 1) commit1(&kv_empty[gt % NST]);
-          if (k + 3 < kend) ok = s_step(k + 3);
-        }
-      } else {
-        // One buffer per tile: S_A(g0) S_B(g0), then per KV tile g and tile
-        // t: PV_t(g), then S_t(g+1) into the same buffer once PV_t(g) is done.
-        for (int tt = 0; ok && tt < 2; ++tt) {
-          if (tt == 0 && !wwait1(&kv_full[g0 % NST], (g0 / NST) & 1)) { ok = false; break; }
-          if (g0 > 0 && !wwait1(&pv_done[tt], (g0 - 1) & 1)) { ok = false; break; }
-          tc::fence_after_sync();
-          issue_s(tt, g0);
-          if (n == 1 && tt == 1) commit1(q_empty);
-        }
-        for (int jj = 0; ok && jj < n; ++jj) {
-          const int gg = g0 + jj;
-          for (int tt = 0; tt < 2; ++tt) {
-            if (!wwait1(&p_full[tt], gg & 1)) { ok = false; break; }
+          issue_pv(tt, gg, jj == 0);
+          if (tt == NT - 1) commit1(&kv_empty[gg % NST]);
+          if (jj + 1 < n) {
+            if (tt == 0 && !wwait1(&kv_full[(gg + 1) % NST], ((gg + 1) / NST) & 1)) { ok = false; break; }
+            if (!wwait1(&pv_done[tt], gg & 1)) { ok = false; break; }
             tc::fence_after_sync();
-            issue_pv(tt, gg, jj == 0);
-            if (tt == 1) commit1(&kv_empty[gg % NST]);
-            if (jj + 1 < n) {
-              if (tt == 0 && !wwait1(&kv_full[(gg + 1) % NST], ((gg + 1) / NST) & 1)) { ok = false; break; }
-              if (!wwait1(&pv_done[tt], gg & 1)) { ok = false; break; }
-              tc::fence_after_sync();
-              issue_s(tt, gg + 1);
-              if (jj + 2 == n && tt == 1) commit1(q_empty);
-            }
+            issue_s(tt, gg + 1);
+            if (jj + 2 == n && tt == NT - 1) commit1(q_empty);
           }
         }
       }
@@ -946,7 +879,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_drain(drain, 0);
   } else {
     // ---------------------------------------------------------------- softmax
-    // 8 warps: tile t = A/B; warp w may access TMEM lanes 32 (w % 4) ...
+    // 4 NT warps: tile t; warp w may access TMEM lanes 32 (w % 4) ...
     const int t = (warp - 2) >> 2;
     const int quad = warp & 3;       // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
@@ -963,14 +896,11 @@ __global__ void __launch_bounds__(320, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
     };
     // wait for PV_t of global KV tile gg
-    auto pv_wait = [&](int gg) -> bool {
-      return C::RING ? wwait(&pv_buf[C::buf_of(t, gg)], C::use_of(t, gg) & 1)
-                     : wwait(&pv_done[t], gg & 1);
-    };
+    auto pv_wait = [&](int gg) -> bool { return wwait(&pv_done[t], gg & 1); };
     int g = 0;   // KV tiles so far
     bool ok = true;
     for (int k = 0; ok && k < n_mine; ++k) {
-      const PfItem it_ = pf_item<KT>(p, item_of(k));
+      const PfItem it_ = pf_item<KT, NT>(p, item_of(k));
       if (it_.n < 0) continue;
       const int n = it_.n;
       const int tl = t * p.QB + rg;    // token within the item
@@ -997,8 +927,8 @@ __global__ void __launch_bounds__(320, 1)
 
       for (int j = 0; j < n; ++j) {
         const int gg = g + j;
-        const int buf = C::buf_of(t, gg);
-        if (!wwait(&s_full[buf], C::use_of(t, gg) & 1)) { ok = false; break; }
+        const int buf = t;
+        if (!wwait(&s_full[buf], gg & 1)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t s_addr = lane_base + C::col_s(buf);
         const int j0 = it_.first + j * KT;
@@ -1070,14 +1000,9 @@ __global__ void __launch_bounds__(320, 1)
         const float2 rsa = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
         const float rs = rsa.x + rsa.y;
 
-        // Two buffers per tile: PV_t(j-1) has completed before O_t is touched
-        // or P_t(j) is handed over (so p_full[t] cannot run two phases ahead
-        // of the MMA warp). With one buffer S_t(j) was issued after PV_t(j-1);
-        // at j = 0 the previous item's epilogue waited for its last PV_t.
-        if (C::RING && j >= 1) {
-          if (!pv_wait(gg - 1)) { ok = false; break; }
-          tc::fence_after_sync();
-        }
+        // S_t(j) was issued after PV_t(j-1) had completed (at j = 0 the
+        // previous item's epilogue waited for its last PV_t), so O_t is free
+        // to touch and p_full[t] cannot run two phases ahead of the MMA warp.
         // Rescale the row's O_t when some row of this warp moved its maximum
         // (warp-uniform branch).
         if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
@@ -1135,11 +1060,12 @@ __global__ void __launch_bounds__(320, 1)
 // ---------------------------------------------------------------------------
 // NT query tiles per CTA for the one-block launch; the persistent launch
 // always runs two.
-template <int D, int NST, int NT>
+template <int D, int NST, int NT, int PERS_NT>
 static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   static_assert(NT >= 2, "tiles per CTA");
   using C = TcCfg<D, NST, NT>;
-  using CP = TcCfg<D, NST, 2>;
+  constexpr int PNT = PERS_NT;   // query tiles per item of the persistent launch
+  using CP = TcCfg<D, NST, PNT>;
   const int G = a.Hq / a.Hkv;
   CUtensorMap tmQ, tmK, tmV;
   const int QB = 128 / G;
@@ -1165,7 +1091,7 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.Hkv = a.Hkv;
   p.G = G;
   p.QB = QB;
-  const int tiles = persistent ? 2 : NT;   // query tiles per item
+  const int tiles = persistent ? PNT : NT;   // query tiles per item
   p.nqb = (a.max_q + tiles * QB - 1) / (tiles * QB);
   p.batch = a.batch;
   const int64_t items = static_cast<int64_t>(p.nqb) * a.Hkv * a.batch;
@@ -1183,7 +1109,7 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
 
-  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST> : prefill_tc_kernel<D, NST, NT>;
+  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST, PNT> : prefill_tc_kernel<D, NST, NT>;
   const int smem = persistent ? CP::SMEM : C::SMEM;
   const int threads = persistent ? CP::THREADS : C::THREADS;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1206,26 +1132,25 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
 
 // Persistent CTAs pay off when items are short (a few KV tiles: a sliding
 // window, short prompts), where the one-block-per-item launch spends much of
-// its time starting and finishing blocks; with long items the one-block
-// launch measured faster (full-causal gpt-oss-shaped prefill 737 against
-// 680 TFLOP/s).
-static bool prefer_persistent(const AttnArgs& a, int kt) {
+// its time starting and finishing blocks.
+static bool prefer_persistent(const AttnArgs& a, int kt, int tiles) {
   const int G = a.Hq / a.Hkv;
-  const int tokens = 2 * (128 / G);   // query tokens per item
+  const int tokens = tiles * (128 / G);   // query tokens per item
   const long long keys = a.window > 0 ? static_cast<long long>(a.window) + tokens
                                       : (a.causal ? a.max_kv / 2 : a.max_kv);
   return keys <= 6LL * kt;
 }
 
-// At d 128 both launches run two tiles per CTA, and the persistent one also
-// wins when every SM gets many items, so that the snake order evens out their
-// lengths: Qwen-shaped prefill (3000 items of 2 x 6000 tokens) 1390 against
-// 1340 TFLOP/s. With few long items per SM (1024 items of a 16-draft decode)
-// the hardware's dynamic block dealing balances better (0.69 against
-// 0.73 ms).
-static bool many_items_per_sm(const AttnArgs& a) {
+// Both launches run the same tiles per CTA (three at d 64, two at d 128), and
+// the persistent one also wins when every SM gets many items, so that the
+// snake order evens out their lengths: full-causal gpt-oss-shaped prefill
+// 846 against 796 TFLOP/s, Qwen-shaped prefill (3000 items of 2 x 6000
+// tokens) 1390 against 1340. With few long items per SM (1024 items of a
+// 16-draft decode) the hardware's dynamic block dealing balances better
+// (0.69 against 0.73 ms).
+static bool many_items_per_sm(const AttnArgs& a, int tiles) {
   const int G = a.Hq / a.Hkv;
-  const long long tokens = 2 * (128 / G);
+  const long long tokens = tiles * (128 / G);
   const long long items = (a.max_q + tokens - 1) / tokens * a.Hkv * a.batch;
   return items >= 16LL * sm_count();
 }
@@ -1238,13 +1163,14 @@ int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
   }
   if (a.d == 64) {
     const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
-                      (kind == SINKATTN_PREFILL_AUTO && prefer_persistent(a, TcCfg<64, 4>::KT));
-    return launch_tc<64, 4, 3>(a, pers, stream);
+                      (kind == SINKATTN_PREFILL_AUTO &&
+                       (prefer_persistent(a, TcCfg<64, 4, 3>::KT, 3) || many_items_per_sm(a, 3)));
+    return launch_tc<64, 4, 3, 3>(a, pers, stream);
   }
   const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
                     (kind == SINKATTN_PREFILL_AUTO &&
-                     (prefer_persistent(a, TcCfg<128, 2>::KT) || many_items_per_sm(a)));
-  return launch_tc<128, 2, 2>(a, pers, stream);
+                     (prefer_persistent(a, TcCfg<128, 2>::KT, 2) || many_items_per_sm(a, 2)));
+  return launch_tc<128, 2, 2, 2>(a, pers, stream);
 }
 
 SINKATTN_DEFINE_SET_HOOKS(set_hooks_prefill_tc)

@@ -251,9 +251,8 @@ SINKATTN_API int sinkattn_set_decode_kernel(int kind);
  * Process-wide choice of the prefill launch (both run the same tcgen05
  * kernel body and give the same results up to floating-point rounding order):
  *   SINKATTN_PREFILL_AUTO (0, default): persistent when the work items are
- *     short (a sliding window, or prompts of a few KV tiles) or, at
- *     head_dim 128, when there are at least 16 items per SM; else one block
- *     per item;
+ *     short (a sliding window, or prompts of a few KV tiles) or when there
+ *     are at least 16 items per SM; else one block per item;
  *   SINKATTN_PREFILL_ONE_BLOCK (1): one thread block per (query block, KV
  *     head, sequence), scheduled by the hardware;
  *   SINKATTN_PREFILL_PERSISTENT (2): one thread block per SM working through
