@@ -841,9 +841,19 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
     };
     int g = 0, qi = 0;   // KV tiles and active items so far
     bool ok = true;
-    for (int k = 0; ok && k < n_mine; ++k) {
-      const PfItem t = pf_item<KT, NT>(p, item_of(k));
-      if (t.n <= 0) continue;
+    // this CTA's next item with KV tiles after item k0 (n_mine when none)
+    auto next_item = [&](int k0, PfItem& t) -> int {
+      for (int k = k0 + 1; k < n_mine; ++k) {
+        t = pf_item<KT, NT>(p, item_of(k));
+        if (t.n > 0) return k;
+      }
+      return n_mine;
+    };
+    PfItem t_nx;
+    int k_nx = next_item(-1, t_nx);
+    while (ok && k_nx < n_mine) {
+      const int k = k_nx;
+      const PfItem t = t_nx;
       if (!wwait1(q_full, qi & 1)) { ok = false; break; }
       const int g0 = g, n = t.n;
       // One buffer per tile: S_t(g0) of every tile, then per KV tile g and
@@ -855,6 +865,9 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
         issue_s(tt, g0);
         if (n == 1 && tt == NT - 1) commit1(q_empty);
       }
+      // the next item's geometry, looked up while this item's first softmax
+      // runs (its sequence offsets are global loads of about a microsecond)
+      k_nx = next_item(k, t_nx);
       for (int jj = 0; ok && jj < n; ++jj) {
         const int gg = g0 + jj;
         for (int tt = 0; tt < NT; ++tt) {
