@@ -1071,21 +1071,17 @@ __global__ void __launch_bounds__(TcCfg<D, NST, NT>::LB_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-// NT query tiles per CTA for the one-block launch; the persistent launch
-// always runs two.
-template <int D, int NST, int NT, int PERS_NT>
+// NT query tiles per CTA, in both launches.
+template <int D, int NST, int NT>
 static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   static_assert(NT >= 2, "tiles per CTA");
   using C = TcCfg<D, NST, NT>;
-  constexpr int PNT = PERS_NT;   // query tiles per item of the persistent launch
-  using CP = TcCfg<D, NST, PNT>;
   const int G = a.Hq / a.Hkv;
   CUtensorMap tmQ, tmK, tmV;
   const int QB = 128 / G;
   int rc = make_q_tmap(&tmQ, a.q, static_cast<uint64_t>(a.total_q), a.Hq, D, G, QB);
   if (rc) return rc;
   const uint64_t rows = kv_map_rows(a);
-  static_assert(C::KT == CP::KT, "both launches tile the keys alike");
   const int box = kv_box_rows(a, C::KT);
   rc = make_rows_tmap(&tmK, a.k, rows, D, box, 128);
   if (rc) return rc;
@@ -1104,7 +1100,7 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.Hkv = a.Hkv;
   p.G = G;
   p.QB = QB;
-  const int tiles = persistent ? PNT : NT;   // query tiles per item
+  const int tiles = NT;   // query tiles per item
   p.nqb = (a.max_q + tiles * QB - 1) / (tiles * QB);
   p.batch = a.batch;
   const int64_t items = static_cast<int64_t>(p.nqb) * a.Hkv * a.batch;
@@ -1122,9 +1118,9 @@ static int launch_tc(const AttnArgs& a, bool persistent, cudaStream_t stream) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
 
-  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST, PNT> : prefill_tc_kernel<D, NST, NT>;
-  const int smem = persistent ? CP::SMEM : C::SMEM;
-  const int threads = persistent ? CP::THREADS : C::THREADS;
+  auto kern = persistent ? prefill_tc_persistent_kernel<D, NST, NT> : prefill_tc_kernel<D, NST, NT>;
+  const int smem = C::SMEM;
+  const int threads = C::THREADS;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -1178,12 +1174,12 @@ int launch_prefill_tc(const AttnArgs& a, int kind, cudaStream_t stream) {
     const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
                       (kind == SINKATTN_PREFILL_AUTO &&
                        (prefer_persistent(a, TcCfg<64, 4, 3>::KT, 3) || many_items_per_sm(a, 3)));
-    return launch_tc<64, 4, 3, 3>(a, pers, stream);
+    return launch_tc<64, 4, 3>(a, pers, stream);
   }
   const bool pers = kind == SINKATTN_PREFILL_PERSISTENT ||
                     (kind == SINKATTN_PREFILL_AUTO &&
                      (prefer_persistent(a, TcCfg<128, 2>::KT, 2) || many_items_per_sm(a, 2)));
-  return launch_tc<128, 2, 2, 2>(a, pers, stream);
+  return launch_tc<128, 2, 2>(a, pers, stream);
 }
 
 SINKATTN_DEFINE_SET_HOOKS(set_hooks_prefill_tc)
