@@ -97,6 +97,12 @@ struct MmaCfg {
   static constexpr int XOUT_STRIDE = D + 4;
   static_assert(FP8 || 16 * RT * XOUT_STRIDE * 4 <= NST * STAGE_BYTES,
                 "partial fits in the tile ring");
+  // Token group tg takes tiles tg, tg + TG, ...; tile i lives in stage i % NST
+  // with barrier phase (i / NST) % 2. Each stage must serve one group only,
+  // which consumes its tiles in order: a stage shared by two groups lets one
+  // of them wait for a tile two phases ahead while the stage's previous tile
+  // is still in flight, and the parity wait would pass on the wrong phase.
+  static_assert(NST % TG == 0, "every ring stage serves one token group");
   // Two resident CTAs per SM: one CTA's prologue (barrier set-up, first TMA
   // round trip, Q fragments) and epilogue overlap the other's streaming.
   static constexpr int MIN_CTAS = 2;
