@@ -39,6 +39,8 @@ FP8_CASES = [
     (5, 1, 16, 1, 128, (1, 40), 8, 0, 1.0),        # short sequences, empty chunks
     (2, 16, 4, 1, 64, (16, 200), 2, 0, 1.0),       # 64 rows
     (1, 1, 8, 8, 64, (2000, 2000), 1, 0, 1.0),     # MHA, one long chunk
+    (2, 3, 64, 8, 64, (3, 900), 4, 50, 1.0),       # 24 rows, window 50: masks in the permuted key order
+    (2, 8, 64, 8, 64, (8, 700), 3, 0, 1.0),        # 64 rows: four row tiles, two token groups
     # head_dim 128 shapes for the tcgen05 kernel (tiles of 16..64 rows, ragged q blocks)
     (3, 4, 64, 4, 128, (4, 900), 3, 0, 1.0),       # 64 rows: the MTP shape
     (2, 5, 32, 4, 128, (5, 1100), 2, 0, 3.0),      # 40 rows, peaky logits
