@@ -66,6 +66,8 @@ PREFILL_CASES = [
     ([150], [150], 16, 1, 64, True, 0, "given", 4.0),                  # peaky logits
     ([81], [81], 32, 2, 128, True, 17, "mixed", 3.0),
     ([1, 2, 3], [1, 2, 3], 4, 1, 128, True, 0, "given", 1.0),          # tiny sequences
+    ([40, 7], [40, 7], 128, 1, 64, True, 0, "given", 1.0),            # G = 128: one token per tile
+    ([33], [60], 32, 1, 128, True, 0, "given", 1.0),                   # G = 32, chunked
 ]
 
 
