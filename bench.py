@@ -594,7 +594,8 @@ def main():
     if rank == 0:
         if detail:
             # kernel names, splits and ncu traffic of the secondary workloads
-            print(json.dumps({"detail": detail}), flush=True)
+            # (stderr: stdout carries the one JSON result line)
+            print(json.dumps({"detail": detail}), file=sys.stderr, flush=True)
         line = {
             "metric": METRIC, "value": _r(value), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": _r(ms),
